@@ -1,0 +1,255 @@
+"""Thin ctypes binding of libattn_a2a.so (include/attn_a2a.h).
+
+Argument marshalling only: tensors become raw pointers, shapes and strides
+become the C structs, the current torch CUDA stream becomes the cudaStream_t.
+Every step of the computation runs in the library's CUDA kernels. There is
+no fallback: if the library is missing, loading raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libattn_a2a.so")
+
+OK, EINVAL, EUNSUPPORTED, ECUDA, ETIMEOUT = 0, 1, 2, 3, 4
+MAX_RANKS = 64
+
+# Every symbol include/attn_a2a.h declares.
+EXPORTED = (
+    "attn_a2a_fwd",
+    "attn_a2a_fwd_ex",
+    "attn_a2a_fwd_contig",
+    "attn_a2a_fwd_contig_ex",
+    "attn_a2a_permute",
+    "attn_a2a_fwd_simt",
+    "attn_a2a_fwd_host",
+    "xstage_probe_run",
+    "attn_a2a_strerror",
+    "attn_a2a_num_sms",
+)
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("H", ctypes.c_int), ("S", ctypes.c_int), ("d", ctypes.c_int)] + [
+        (n, ctypes.c_longlong)
+        for n in ("q_sb", "q_sh", "q_ss", "k_sb", "k_sh", "k_ss", "v_sb", "v_sh", "v_ss")
+    ]
+
+
+class Opts(ctypes.Structure):
+    _fields_ = [
+        ("store_kind", ctypes.c_int),
+        ("grid", ctypes.c_int),
+        ("timeout_ns", ctypes.c_longlong),
+        ("inject_stall", ctypes.c_int),
+        ("reserved", ctypes.c_int * 3),
+    ]
+
+
+class ProbeCfg(ctypes.Structure):
+    _fields_ = [
+        ("K", ctypes.c_int),
+        ("rounds", ctypes.c_int),
+        ("V_bytes", ctypes.c_longlong),
+        ("G_ns", ctypes.c_longlong),
+        ("store_kind", ctypes.c_int),
+        ("gap_kind", ctypes.c_int),
+        ("dst", ctypes.c_void_p),
+        ("dst_bytes", ctypes.c_longlong),
+        ("stamps", ctypes.c_void_p),
+        ("fma_iters", ctypes.c_longlong),
+    ]
+
+
+class AttnA2AError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {strerror(code)} (status {code})")
+        self.code = code
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load the shared library (once). Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"{path} is missing: build it with `python -m attention_all_layout_gb300.build` "
+            "(there is no CPU or PyTorch fallback)"
+        )
+    lib = ctypes.CDLL(path)
+    vp, cint = ctypes.c_void_p, ctypes.c_int
+    pp = ctypes.POINTER(ctypes.c_void_p)
+    shp = ctypes.POINTER(Shape)
+    opt = ctypes.POINTER(Opts)
+    lib.attn_a2a_fwd.argtypes = [vp, vp, vp, shp, cint, ctypes.c_float, pp, vp, vp]
+    lib.attn_a2a_fwd_ex.argtypes = [vp, vp, vp, shp, cint, ctypes.c_float, pp, vp, opt, vp]
+    lib.attn_a2a_fwd_contig.argtypes = [vp, vp, vp, shp, ctypes.c_float, vp, vp, vp]
+    lib.attn_a2a_fwd_contig_ex.argtypes = [vp, vp, vp, shp, ctypes.c_float, vp, vp, opt, vp]
+    lib.attn_a2a_permute.argtypes = [vp, shp, cint, pp, vp]
+    lib.attn_a2a_fwd_simt.argtypes = [vp, vp, vp, shp, cint, ctypes.c_float, pp, vp]
+    lib.attn_a2a_fwd_host.argtypes = [vp, vp, vp, shp, cint, ctypes.c_float, vp, vp, vp, pp, pp, vp, vp]
+    lib.xstage_probe_run.argtypes = [ctypes.POINTER(ProbeCfg), vp]
+    lib.attn_a2a_strerror.argtypes = [cint]
+    lib.attn_a2a_strerror.restype = ctypes.c_char_p
+    lib.attn_a2a_num_sms.argtypes = []
+    for name in EXPORTED:
+        if name != "attn_a2a_strerror":
+            getattr(lib, name).restype = cint
+    _lib = lib
+    return lib
+
+
+def strerror(code: int) -> str:
+    return load().attn_a2a_strerror(int(code)).decode()
+
+
+def num_sms() -> int:
+    return int(load().attn_a2a_num_sms())
+
+
+# ------------------------------------------------------------------ marshalling helpers
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream if torch.cuda.is_available() else None
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def shape_of(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor) -> Shape:
+    """attn_a2a_shape of [B, H, S, d] tensors (innermost stride must be 1)."""
+    B, H, S, d = q.shape
+    for t in (q, k, v):
+        if t.dim() != 4 or tuple(t.shape) != (B, H, S, d):
+            raise ValueError("q, k, v must share one [B, H, S, d] shape")
+        if t.dtype != torch.bfloat16:
+            raise ValueError("q, k, v must be bf16")
+        if d > 0 and t.stride(3) != 1 and t.numel() > 0:
+            raise ValueError("the head dimension must be contiguous")
+    return Shape(B, H, S, d, *q.stride()[:3], *k.stride()[:3], *v.stride()[:3])
+
+
+def plain_shape(B: int, H: int, S: int, d: int) -> Shape:
+    sb, sh, ss = H * S * d, S * d, d
+    return Shape(B, H, S, d, sb, sh, ss, sb, sh, ss, sb, sh, ss)
+
+
+def chunk_sizes(S: int, P: int) -> list[int]:
+    """Rows of each of the P sequence chunks (larger chunks first)."""
+    base, rem = divmod(S, P)
+    return [base + (1 if j < rem else 0) for j in range(P)]
+
+
+def alloc_partitions(B: int, S: int, H: int, d: int, P: int, device="cuda", fill=None):
+    """P contiguous bf16 partitions [B, c_j, H, d] on `device`."""
+    parts = []
+    for c in chunk_sizes(S, P):
+        t = torch.empty((B, c, H, d), dtype=torch.bfloat16, device=device)
+        if fill is not None:
+            t.fill_(fill)
+        parts.append(t)
+    return parts
+
+
+def _ptr_array(tensors: Sequence[Optional[torch.Tensor]]):
+    arr = (ctypes.c_void_p * max(1, len(tensors)))()
+    for i, t in enumerate(tensors):
+        arr[i] = None if (t is None or t.numel() == 0) else t.data_ptr()
+    return arr
+
+
+def _opts(store_kind=0, grid=0, timeout_ns=0, inject_stall=0) -> Opts:
+    return Opts(store_kind, grid, timeout_ns, inject_stall, (ctypes.c_int * 3)(0, 0, 0))
+
+
+def _check(code: int, what: str, check: bool) -> int:
+    if check and code != OK:
+        raise AttnA2AError(code, what)
+    return code
+
+
+# ------------------------------------------------------------------ entry points (same names as the C ABI)
+def attn_a2a_fwd(q, k, v, P: int, scale: float, out_partitions, dev_status=None, stream=None,
+                 store_kind: int = 0, grid: int = 0, timeout_ns: int = 0, inject_stall: int = 0,
+                 check: bool = True) -> int:
+    """Fused attention + head->sequence all-to-all into `out_partitions` (P tensors [B,c_j,H,d])."""
+    lib = load()
+    shp = shape_of(q, k, v)
+    parts = _ptr_array(out_partitions)
+    opts = _opts(store_kind, grid, timeout_ns, inject_stall)
+    rc = lib.attn_a2a_fwd_ex(_ptr(q), _ptr(k), _ptr(v), ctypes.byref(shp), int(P), float(scale), parts,
+                             _ptr(dev_status), ctypes.byref(opts), _stream(stream))
+    return _check(rc, "attn_a2a_fwd", check)
+
+
+def attn_a2a_fwd_contig(q, k, v, scale: float, out, dev_status=None, stream=None, store_kind: int = 0,
+                        grid: int = 0, timeout_ns: int = 0, check: bool = True) -> int:
+    """The same kernel with a contiguous [B, H, S, d] output ("attention alone")."""
+    lib = load()
+    shp = shape_of(q, k, v)
+    opts = _opts(store_kind, grid, timeout_ns, 0)
+    rc = lib.attn_a2a_fwd_contig_ex(_ptr(q), _ptr(k), _ptr(v), ctypes.byref(shp), float(scale), _ptr(out),
+                                    _ptr(dev_status), ctypes.byref(opts), _stream(stream))
+    return _check(rc, "attn_a2a_fwd_contig", check)
+
+
+def attn_a2a_permute(o, P: int, out_partitions, stream=None, check: bool = True) -> int:
+    """Separate all-to-all copy of a contiguous [B, H, S, d] tensor into the partitions."""
+    lib = load()
+    B, H, S, d = o.shape
+    shp = plain_shape(B, H, S, d)
+    rc = lib.attn_a2a_permute(_ptr(o), ctypes.byref(shp), int(P), _ptr_array(out_partitions), _stream(stream))
+    return _check(rc, "attn_a2a_permute", check)
+
+
+def attn_a2a_fwd_simt(q, k, v, P: int, scale: float, out_partitions, stream=None, check: bool = True) -> int:
+    """Slow SIMT debug path with the same partition epilogue."""
+    lib = load()
+    shp = shape_of(q, k, v)
+    rc = lib.attn_a2a_fwd_simt(_ptr(q), _ptr(k), _ptr(v), ctypes.byref(shp), int(P), float(scale),
+                               _ptr_array(out_partitions), _stream(stream))
+    return _check(rc, "attn_a2a_fwd_simt", check)
+
+
+def attn_a2a_fwd_host(hq, hk, hv, P: int, scale: float, dq, dk, dv, dparts, hparts, dev_status=None,
+                      stream=None, check: bool = True) -> int:
+    """Host-memory variant: H2D copies, fused kernel, D2H copies, all enqueued on `stream`."""
+    lib = load()
+    B, H, S, d = hq.shape
+    shp = plain_shape(B, H, S, d)
+    rc = lib.attn_a2a_fwd_host(_ptr(hq), _ptr(hk), _ptr(hv), ctypes.byref(shp), int(P), float(scale),
+                               _ptr(dq), _ptr(dk), _ptr(dv), _ptr_array(dparts), _ptr_array(hparts),
+                               _ptr(dev_status), _stream(stream))
+    return _check(rc, "attn_a2a_fwd_host", check)
+
+
+def xstage_probe_run(K: int, rounds: int, V_bytes: int, G_ns: int, dst: torch.Tensor, stamps: torch.Tensor,
+                     store_kind: int = 0, gap_kind: int = 0, fma_iters: int = 0, stream=None,
+                     check: bool = True) -> int:
+    """One Burst-Gap probe launch; per-round stamps land in `stamps` (int64 [K, rounds, 3])."""
+    lib = load()
+    cfg = ProbeCfg(int(K), int(rounds), int(V_bytes), int(G_ns), int(store_kind), int(gap_kind),
+                   _ptr(dst), dst.numel() * dst.element_size(), _ptr(stamps), int(fma_iters))
+    rc = lib.xstage_probe_run(ctypes.byref(cfg), _stream(stream))
+    return _check(rc, "xstage_probe_run", check)
+
+
+def attn_a2a_strerror(code: int) -> str:
+    return strerror(code)
+
+
+def attn_a2a_num_sms() -> int:
+    return num_sms()

@@ -1,0 +1,262 @@
+// C ABI of libattn_a2a.so: argument validation, the chunk rule of the
+// sequence-sharded partitions, and dispatch to the kernels' launchers.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "../../include/attn_a2a.h"
+#include "internal.h"
+
+namespace attn_a2a {
+
+int num_sms_current_device() {
+  static int cache[128] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return 0;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Span {
+  uintptr_t lo, hi;  // [lo, hi)
+};
+
+bool overlaps(const Span& a, const Span& b) { return a.lo < b.hi && b.lo < a.hi; }
+
+// Bytes spanned by a strided [B, H, S, d] bf16 tensor.
+Span tensor_span(const void* p, int B, int H, int S, int d, long long sb, long long sh, long long ss) {
+  const long long last = (B - 1) * sb + (H - 1) * sh + (S - 1) * ss + d;
+  const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+  return Span{lo, lo + static_cast<uintptr_t>(last) * 2u};
+}
+
+bool stride_ok(long long s, int extent) {
+  if (extent <= 1) return true;  // never used to address memory
+  return s > 0 && (s % 8) == 0 && s * 2 < (1ll << 40);
+}
+
+// Shape, scale and input pointers. Sets *empty when there is nothing to do.
+int check_inputs(const void* q, const void* k, const void* v, const attn_a2a_shape* shp, float scale,
+                 bool* empty) {
+  if (shp == nullptr) return ATTN_A2A_EINVAL;
+  if (shp->B < 0 || shp->H < 0 || shp->S < 0 || shp->d <= 0) return ATTN_A2A_EINVAL;
+  if (!std::isfinite(scale) || scale < 0.f) return ATTN_A2A_EINVAL;
+  if (shp->d != 64 && shp->d != 128) return ATTN_A2A_EUNSUPPORTED;
+  *empty = (shp->B == 0 || shp->H == 0 || shp->S == 0);
+  if (*empty) return ATTN_A2A_OK;
+  if (static_cast<long long>(shp->B) * shp->H * ((shp->S + 255) / 256) > (1ll << 30))
+    return ATTN_A2A_EUNSUPPORTED;  // work-item count must fit an int
+  if (q == nullptr || k == nullptr || v == nullptr) return ATTN_A2A_EINVAL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return ATTN_A2A_EINVAL;
+  const long long st[9] = {shp->q_sb, shp->q_sh, shp->q_ss, shp->k_sb, shp->k_sh,
+                           shp->k_ss, shp->v_sb, shp->v_sh, shp->v_ss};
+  const int ext[3] = {shp->B, shp->H, shp->S};
+  for (int i = 0; i < 9; ++i)
+    if (!stride_ok(st[i], ext[i % 3])) return ATTN_A2A_EINVAL;
+  return ATTN_A2A_OK;
+}
+
+// Partition pointers and the chunk rule: chunk j has floor(S/P) rows plus one
+// for j < S mod P (torch.tensor_split).
+int make_partitions(const attn_a2a_shape& shp, int P, void* const* parts, EpiParams* e) {
+  if (P < 1 || P > kMaxRanks) return ATTN_A2A_EINVAL;
+  if (shp.H % P != 0) return ATTN_A2A_EINVAL;
+  if (parts == nullptr) return ATTN_A2A_EINVAL;
+  std::memset(e, 0, sizeof(*e));
+  e->P = P;
+  e->cbase = shp.S / P;
+  e->crem = shp.S % P;
+  for (int j = 0; j < P; ++j) {
+    const int c = e->cbase + (j < e->crem ? 1 : 0);
+    const bool has_bytes = c > 0 && shp.B > 0 && shp.H > 0;
+    if (has_bytes && (parts[j] == nullptr || !aligned16(parts[j]))) return ATTN_A2A_EINVAL;
+    e->part[j] = parts[j];
+  }
+  return ATTN_A2A_OK;
+}
+
+bool partitions_alias_inputs(const attn_a2a_shape& shp, const EpiParams& e, const Span* in, int nin) {
+  for (int j = 0; j < e.P; ++j) {
+    const int c = e.cbase + (j < e.crem ? 1 : 0);
+    if (c == 0) continue;
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(e.part[j]);
+    const Span out{lo, lo + static_cast<uintptr_t>(shp.B) * c * shp.H * shp.d * 2u};
+    for (int i = 0; i < nin; ++i)
+      if (overlaps(out, in[i])) return true;
+  }
+  return false;
+}
+
+attn_a2a_opts default_opts() {
+  attn_a2a_opts o;
+  std::memset(&o, 0, sizeof(o));
+  return o;
+}
+
+int fwd_common(const void* q, const void* k, const void* v, const attn_a2a_shape* shp, int P,
+               float scale, void* const* out_partitions, void* out_contig, bool a2a, int* dev_status,
+               const attn_a2a_opts* opts, void* stream) {
+  bool empty = false;
+  int rc = check_inputs(q, k, v, shp, scale, &empty);
+  if (rc != ATTN_A2A_OK) return rc;
+  if (opts != nullptr && (opts->store_kind < 0 || opts->store_kind > 1 || opts->grid < 0 ||
+                          opts->timeout_ns < 0 || opts->inject_stall < 0 || opts->inject_stall > 1))
+    return ATTN_A2A_EINVAL;
+  EpiParams epi;
+  std::memset(&epi, 0, sizeof(epi));
+  if (a2a) {
+    rc = make_partitions(*shp, P, out_partitions, &epi);
+    if (rc != ATTN_A2A_OK) return rc;
+  } else {
+    epi.P = 1;
+    epi.cbase = shp->S;
+    epi.out = out_contig;
+  }
+  if (empty) return ATTN_A2A_OK;
+  const Span in[3] = {
+      tensor_span(q, shp->B, shp->H, shp->S, shp->d, shp->q_sb, shp->q_sh, shp->q_ss),
+      tensor_span(k, shp->B, shp->H, shp->S, shp->d, shp->k_sb, shp->k_sh, shp->k_ss),
+      tensor_span(v, shp->B, shp->H, shp->S, shp->d, shp->v_sb, shp->v_sh, shp->v_ss)};
+  if (a2a) {
+    if (partitions_alias_inputs(*shp, epi, in, 3)) return ATTN_A2A_EINVAL;
+  } else {
+    if (out_contig == nullptr || !aligned16(out_contig)) return ATTN_A2A_EINVAL;
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(out_contig);
+    const Span out{lo, lo + static_cast<uintptr_t>(shp->B) * shp->H * shp->S * shp->d * 2u};
+    for (const Span& s : in)
+      if (overlaps(out, s)) return ATTN_A2A_EINVAL;
+  }
+  const attn_a2a_opts o = opts ? *opts : default_opts();
+  return launch_fa_tc(q, k, v, *shp, scale, a2a, epi, dev_status, o, static_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+}  // namespace attn_a2a
+
+using namespace attn_a2a;
+
+extern "C" {
+
+const char* attn_a2a_strerror(int status) {
+  switch (status) {
+    case ATTN_A2A_OK: return "ok";
+    case ATTN_A2A_EINVAL: return "invalid argument";
+    case ATTN_A2A_EUNSUPPORTED: return "unsupported configuration";
+    case ATTN_A2A_ECUDA: return "CUDA error";
+    case ATTN_A2A_ETIMEOUT: return "bounded in-kernel wait expired";
+    default: return "unknown status";
+  }
+}
+
+int attn_a2a_num_sms(void) { return num_sms_current_device(); }
+
+int attn_a2a_fwd_ex(const void* q, const void* k, const void* v, const attn_a2a_shape* shp, int P,
+                    float scale, void* const* out_partitions, int* dev_status,
+                    const attn_a2a_opts* opts, void* stream) {
+  return fwd_common(q, k, v, shp, P, scale, out_partitions, nullptr, true, dev_status, opts, stream);
+}
+
+int attn_a2a_fwd(const void* q, const void* k, const void* v, const attn_a2a_shape* shp, int P,
+                 float scale, void* const* out_partitions, int* dev_status, void* stream) {
+  return fwd_common(q, k, v, shp, P, scale, out_partitions, nullptr, true, dev_status, nullptr, stream);
+}
+
+int attn_a2a_fwd_contig_ex(const void* q, const void* k, const void* v, const attn_a2a_shape* shp,
+                           float scale, void* out, int* dev_status, const attn_a2a_opts* opts,
+                           void* stream) {
+  return fwd_common(q, k, v, shp, 1, scale, nullptr, out, false, dev_status, opts, stream);
+}
+
+int attn_a2a_fwd_contig(const void* q, const void* k, const void* v, const attn_a2a_shape* shp,
+                        float scale, void* out, int* dev_status, void* stream) {
+  return fwd_common(q, k, v, shp, 1, scale, nullptr, out, false, dev_status, nullptr, stream);
+}
+
+int attn_a2a_permute(const void* o, const attn_a2a_shape* shp, int P, void* const* out_partitions,
+                     void* stream) {
+  if (shp == nullptr || shp->B < 0 || shp->H < 0 || shp->S < 0) return ATTN_A2A_EINVAL;
+  if (shp->d != 64 && shp->d != 128) return ATTN_A2A_EUNSUPPORTED;
+  EpiParams epi;
+  int rc = make_partitions(*shp, P, out_partitions, &epi);
+  if (rc != ATTN_A2A_OK) return rc;
+  if (static_cast<long long>(shp->B) * shp->H * shp->S == 0) return ATTN_A2A_OK;
+  if (o == nullptr || !aligned16(o)) return ATTN_A2A_EINVAL;
+  const uintptr_t lo = reinterpret_cast<uintptr_t>(o);
+  const Span in{lo, lo + static_cast<uintptr_t>(shp->B) * shp->H * shp->S * shp->d * 2u};
+  if (partitions_alias_inputs(*shp, epi, &in, 1)) return ATTN_A2A_EINVAL;
+  return launch_permute(o, *shp, epi, static_cast<cudaStream_t>(stream));
+}
+
+int attn_a2a_fwd_simt(const void* q, const void* k, const void* v, const attn_a2a_shape* shp, int P,
+                      float scale, void* const* out_partitions, void* stream) {
+  bool empty = false;
+  int rc = check_inputs(q, k, v, shp, scale, &empty);
+  if (rc != ATTN_A2A_OK) return rc;
+  EpiParams epi;
+  rc = make_partitions(*shp, P, out_partitions, &epi);
+  if (rc != ATTN_A2A_OK) return rc;
+  if (empty) return ATTN_A2A_OK;
+  if (shp->H > 65535 || shp->B > 65535) return ATTN_A2A_EUNSUPPORTED;
+  return launch_fa_simt(q, k, v, *shp, scale, epi, static_cast<cudaStream_t>(stream));
+}
+
+int attn_a2a_fwd_host(const void* hq, const void* hk, const void* hv, const attn_a2a_shape* shp, int P,
+                      float scale, void* dq, void* dk, void* dv, void* const* dparts,
+                      void* const* hparts, int* dev_status, void* stream) {
+  if (shp == nullptr) return ATTN_A2A_EINVAL;
+  if (hq == nullptr || hk == nullptr || hv == nullptr || hparts == nullptr) return ATTN_A2A_EINVAL;
+  // The device copies are contiguous [B, H, S, d].
+  attn_a2a_shape s = *shp;
+  s.q_ss = s.k_ss = s.v_ss = s.d;
+  s.q_sh = s.k_sh = s.v_sh = static_cast<long long>(s.S) * s.d;
+  s.q_sb = s.k_sb = s.v_sb = static_cast<long long>(s.H) * s.S * s.d;
+  bool empty = false;
+  int rc = check_inputs(dq, dk, dv, &s, scale, &empty);
+  if (rc != ATTN_A2A_OK) return rc;
+  EpiParams epi;
+  rc = make_partitions(s, P, dparts, &epi);
+  if (rc != ATTN_A2A_OK) return rc;
+  if (empty) return ATTN_A2A_OK;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t bytes = static_cast<size_t>(s.B) * s.H * s.S * s.d * 2u;
+  if (cudaMemcpyAsync(dq, hq, bytes, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(dk, hk, bytes, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+      cudaMemcpyAsync(dv, hv, bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return ATTN_A2A_ECUDA;
+  rc = fwd_common(dq, dk, dv, &s, P, scale, dparts, nullptr, true, dev_status, nullptr, stream);
+  if (rc != ATTN_A2A_OK) return rc;
+  for (int j = 0; j < P; ++j) {
+    const int c = epi.cbase + (j < epi.crem ? 1 : 0);
+    if (c == 0) continue;
+    if (hparts[j] == nullptr) return ATTN_A2A_EINVAL;
+    const size_t pb = static_cast<size_t>(s.B) * c * s.H * s.d * 2u;
+    if (cudaMemcpyAsync(hparts[j], dparts[j], pb, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+      return ATTN_A2A_ECUDA;
+  }
+  return ATTN_A2A_OK;
+}
+
+int xstage_probe_run(const xstage_probe_cfg* cfg, void* stream) {
+  if (cfg == nullptr) return ATTN_A2A_EINVAL;
+  const xstage_probe_cfg& c = *cfg;
+  if (c.K < 1 || c.K > 1024 || c.rounds < 1) return ATTN_A2A_EINVAL;
+  if (c.V_bytes <= 0 || c.V_bytes % (4096ll * c.K) != 0) return ATTN_A2A_EINVAL;
+  if (c.dst_bytes < c.V_bytes || c.dst == nullptr || !aligned16(c.dst)) return ATTN_A2A_EINVAL;
+  if (c.G_ns < 0 || c.store_kind < 0 || c.store_kind > 1 || c.gap_kind < 0 || c.gap_kind > 1)
+    return ATTN_A2A_EINVAL;
+  if (c.gap_kind == 1 && c.fma_iters < 0) return ATTN_A2A_EINVAL;
+  if (c.stamps == nullptr || (reinterpret_cast<uintptr_t>(c.stamps) & 7u) != 0) return ATTN_A2A_EINVAL;
+  return launch_probe(c, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,403 @@
+// Fused attention forward + post-attention all-to-all epilogue on tcgen05.
+//
+// X-Stage pages ("Key Contributions", FlashAttention-A2A piggybacking;
+// "Results", FlashAttention-A2A optimisation): the owner of each output tile
+// stores it straight into its destination layout and immediately resumes the
+// Q loop of its next tile; there is no dedicated communication warp or SM and
+// no separate permute pass. Here the tile owner is the softmax warpgroup that
+// holds the tile's rows: it normalises its O rows, issues their stores into
+// the sequence-sharded partitions and goes back to the next work item's
+// softmax, while the stores drain (the X-stage) behind the next Q loop.
+//
+// CTA layout (384 threads, one CTA per SM, persistent):
+//   warp 0      TMA producer: Q tiles once per work item, then K_j, V_j
+//               through a ring of shared-memory stages
+//   warp 1      MMA issuer (one thread) and TMEM allocator
+//   warps 2-3   idle
+//   warps 4-7   softmax/correction/epilogue for query tile 0 (128 rows)
+//   warps 8-11  the same for query tile 1
+// A work item is (b, h, pair of adjacent 128-row query blocks), so each K/V
+// tile read from L2 serves 256 query rows.
+//
+// Tensor memory (512 columns): S0 [0,128), S1 [128,256) fp32 scores; the
+// bf16 probabilities P_t are written over the first 64 columns of S_t;
+// O0 [256,256+d), O1 [256+d, 256+2d) fp32 accumulators.
+//
+// MMA order per key block j (skewed so each softmax has two MMAs of slack):
+//   S0_j = Q0 K_j^T ; O1 += P1_{j-1} V_{j-1} ; S1_j = Q1 K_j^T ; O0 += P0_j V_j
+// and a final O1 += P1 V after the loop. Because tcgen05 operations of one
+// thread complete in order, the commit after S_t_j also means that the
+// previous P_t V product is done, so the softmax role may rescale O_t in
+// place before it publishes P_t_j.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "epilogue.cuh"
+#include "ptx.cuh"
+
+namespace attn_a2a {
+namespace tc {
+
+constexpr int kBM = 128;  // query rows per tile
+constexpr int kBN = 128;  // keys per block
+constexpr int kThreads = 384;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: keep a stale row max until it lags by 2^8
+
+template <int D>
+struct Cfg {
+  static_assert(D == 64 || D == 128, "head dim");
+  static constexpr int NSTAGE = (D == 128) ? 4 : 6;
+  static constexpr int TILE_BYTES = 128 * D * 2;  // one Q, K or V tile (128 rows x d bf16)
+  static constexpr int ATOM_BYTES = 128 * 128;    // 128 rows x one 128-byte swizzle column
+  static constexpr int Q_OFF = 0;
+  static constexpr int KV_OFF = 2 * TILE_BYTES;
+  static constexpr int BAR_OFF = KV_OFF + NSTAGE * TILE_BYTES;
+  // barrier slots
+  static constexpr int QF = 0, QE = 2, SF = 4, PF = 6, OF = 8, OE = 10, KVF = 12;
+  static constexpr int KVE = KVF + NSTAGE;
+  static constexpr int DONE = KVE + NSTAGE;
+  static constexpr int NBAR = DONE + 1;
+  static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
+  static constexpr int SMEM_USED = MISC_OFF + 16;
+  static constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack for 1024-byte alignment
+};
+
+struct Params {
+  int B, H, S;
+  int nblk;   // ceil(S / 128): query blocks per head = key blocks
+  int npair;  // ceil(nblk / 2): work items per head
+  int total;  // B * H * npair
+  float scale_log2;
+  int* dev_status;
+  unsigned long long timeout_ns;
+  int inject_stall;
+  int store_kind;
+  EpiParams epi;
+};
+
+struct Item {
+  int b, h, pair;
+};
+
+__device__ __forceinline__ Item decode_item(const Params& p, int item) {
+  Item it;
+  it.pair = item % p.npair;
+  const int bh = item / p.npair;
+  it.h = bh % p.H;
+  it.b = bh / p.H;
+  return it;
+}
+
+// ------------------------------------------------------------------ producer
+template <int D>
+__device__ void producer_role(const Params& p, const CUtensorMap* tmQ, const CUtensorMap* tmK,
+                              const CUtensorMap* tmV, uint32_t sbase, uint32_t bar0,
+                              const WaitCtl& w) {
+  using C = Cfg<D>;
+  auto BAR = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
+  const uint64_t pol_kv = l2_policy_evict_last();  // K/V are re-read by every query tile of the head
+  const uint64_t pol_q = l2_policy_evict_first();  // each Q tile is read once
+  uint32_t kv_it = 0;
+  uint32_t q_loads[2] = {0, 0};
+  bool ok = true;
+  int it = 0;
+  for (int item = blockIdx.x; ok && item < p.total; item += gridDim.x, ++it) {
+    const Item wi = decode_item(p, item);
+    auto load_q = [&](int t) -> bool {
+      if (!mbar_wait(BAR(C::QE + t), (it & 1) ^ 1, w)) return false;
+      mbar_arrive_expect_tx(BAR(C::QF + t), C::TILE_BYTES);
+      const uint32_t dst = sbase + C::Q_OFF + t * C::TILE_BYTES;
+      const int row = (2 * wi.pair + t) * kBM;
+#pragma unroll
+      for (int a = 0; a < D / 64; ++a)
+        tma_load_4d(dst + a * C::ATOM_BYTES, tmQ, BAR(C::QF + t), a * 64, row, wi.h, wi.b, pol_q);
+      ++q_loads[t];
+      return true;
+    };
+    auto load_kv = [&](const CUtensorMap* m, int j) -> bool {
+      const uint32_t s = kv_it % C::NSTAGE;
+      const uint32_t ph = (kv_it / C::NSTAGE) & 1;
+      if (!mbar_wait(BAR(C::KVE + s), ph ^ 1, w)) return false;
+      mbar_arrive_expect_tx(BAR(C::KVF + s), C::TILE_BYTES);
+      const uint32_t dst = sbase + C::KV_OFF + s * C::TILE_BYTES;
+#pragma unroll
+      for (int a = 0; a < D / 64; ++a)
+        tma_load_4d(dst + a * C::ATOM_BYTES, m, BAR(C::KVF + s), a * 64, j * kBN, wi.h, wi.b, pol_kv);
+      ++kv_it;
+      return true;
+    };
+    ok = load_q(0) && load_kv(tmK, 0) && load_q(1) && load_kv(tmV, 0);
+    for (int j = 1; ok && j < p.nblk; ++j) ok = load_kv(tmK, j) && load_kv(tmV, j);
+  }
+  if (!ok) {
+    // Aborting: wait (bounded) for the copies this thread started, so none
+    // lands in shared memory after the CTA has exited.
+    const uint32_t n = kv_it < static_cast<uint32_t>(C::NSTAGE) ? kv_it : C::NSTAGE;
+    for (uint32_t i = 0; i < n; ++i) {
+      const uint32_t idx = kv_it - 1 - i;
+      mbar_wait_drain(BAR(C::KVF + idx % C::NSTAGE), (idx / C::NSTAGE) & 1, 100000000ull);
+    }
+    for (int t = 0; t < 2; ++t)
+      if (q_loads[t] > 0) mbar_wait_drain(BAR(C::QF + t), (q_loads[t] - 1) & 1, 100000000ull);
+  }
+}
+
+// ------------------------------------------------------------------ MMA issuer
+template <int D>
+__device__ void mma_role(const Params& p, uint32_t sbase, uint32_t bar0, uint32_t tmem,
+                         const WaitCtl& w) {
+  using C = Cfg<D>;
+  auto BAR = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
+  constexpr uint32_t kIdescQK = idesc_bf16_f32(kBM, kBN, false, false);  // Q, K both K-major
+  constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, D, false, true);     // V is MN-major (d contiguous)
+  uint32_t kv_it = 0;
+  uint32_t pf_cnt[2] = {0, 0};
+  bool ok = true;
+  int it = 0;
+
+  auto issue_qk = [&](int t, uint32_t sK) {
+    const uint32_t qa = sbase + C::Q_OFF + t * C::TILE_BYTES;
+    const uint32_t kb = sbase + C::KV_OFF + sK * C::TILE_BYTES;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const uint32_t off = (kk / 4) * C::ATOM_BYTES + (kk % 4) * 32;
+      umma_ss(tmem + t * 128, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
+              kIdescQK, kk > 0 ? 1u : 0u);
+    }
+  };
+  // O_t (+)= P_t V_j. Returns false on abort.
+  auto issue_pv = [&](int t, int j, uint32_t sV) -> bool {
+    if (!mbar_wait(BAR(C::PF + t), pf_cnt[t] & 1, w)) return false;
+    ++pf_cnt[t];
+    if (j == 0 && !mbar_wait(BAR(C::OE + t), (it & 1) ^ 1, w)) return false;
+    tc_fence_after();
+    const uint32_t vb = sbase + C::KV_OFF + sV * C::TILE_BYTES;
+#pragma unroll
+    for (int kk = 0; kk < kBN / 16; ++kk) {
+      umma_ts(tmem + 256 + t * D, tmem + t * 128 + kk * 8,
+              sdesc_sw128(vb + kk * 2048, C::ATOM_BYTES, 1024), kIdescPV,
+              (j > 0 || kk > 0) ? 1u : 0u);
+    }
+    if (t == 1) umma_commit(BAR(C::KVE + sV));  // V_j now read by both tiles
+    if (j == p.nblk - 1) umma_commit(BAR(C::OF + t));
+    return true;
+  };
+
+  for (int item = blockIdx.x; ok && item < p.total; item += gridDim.x, ++it) {
+    ok = mbar_wait(BAR(C::QF + 0), it & 1, w) && mbar_wait(BAR(C::QF + 1), it & 1, w);
+    if (!ok) break;
+    tc_fence_after();
+    uint32_t sVprev = 0;
+    for (int j = 0; j < p.nblk; ++j) {
+      const uint32_t sK = kv_it % C::NSTAGE;
+      if (!mbar_wait(BAR(C::KVF + sK), (kv_it / C::NSTAGE) & 1, w)) { ok = false; break; }
+      tc_fence_after();
+      issue_qk(0, sK);
+      umma_commit(BAR(C::SF + 0));
+      if (j > 0 && !issue_pv(1, j - 1, sVprev)) { ok = false; break; }
+      issue_qk(1, sK);
+      umma_commit(BAR(C::SF + 1));
+      umma_commit(BAR(C::KVE + sK));  // K_j read by both tiles
+      if (j == p.nblk - 1) {
+        umma_commit(BAR(C::QE + 0));
+        umma_commit(BAR(C::QE + 1));
+      }
+      ++kv_it;
+      const uint32_t sV = kv_it % C::NSTAGE;
+      if (!mbar_wait(BAR(C::KVF + sV), (kv_it / C::NSTAGE) & 1, w)) { ok = false; break; }
+      if (!issue_pv(0, j, sV)) { ok = false; break; }
+      sVprev = sV;
+      ++kv_it;
+    }
+    if (ok && !issue_pv(1, p.nblk - 1, sVprev)) ok = false;
+  }
+  if (!ok) {
+    // Aborting: let every MMA already issued finish before TMEM is freed.
+    umma_commit(BAR(C::DONE));
+    mbar_wait_drain(BAR(C::DONE), 0, 100000000ull);
+  }
+}
+
+// ------------------------------------------------------------------ softmax / epilogue
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+template <int D, bool A2A>
+__device__ void softmax_role(const Params& p, int t, uint32_t bar0, uint32_t tmem, const WaitCtl& w) {
+  using C = Cfg<D>;
+  auto BAR = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int r = (warp & 3) * 32 + lane;  // this thread's row of the tile = its TMEM lane
+  const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+  const uint32_t tS = tmem + lane_off + t * 128;
+  const uint32_t tO = tmem + lane_off + 256 + t * D;
+  const float sl2 = p.scale_log2;
+  uint32_t sf_cnt = 0;
+  int it = 0;
+  for (int item = blockIdx.x; item < p.total; item += gridDim.x, ++it) {
+    const Item wi = decode_item(p, item);
+    const int srow = (2 * wi.pair + t) * kBM + r;
+    float m_used = -INFINITY;
+    float l = 0.f;
+    for (int j = 0; j < p.nblk; ++j) {
+      const bool got = __all_sync(0xffffffffu, mbar_wait(BAR(C::SF + t), sf_cnt & 1, w));
+      if (!got) return;
+      ++sf_cnt;
+      tc_fence_after();
+      uint32_t sr[128];
+      tmem_ld_x128(tS, sr);
+      const int valid = p.S - j * kBN;  // keys of this block that exist (>= 128 except at the end)
+      float mx = -INFINITY;
+      if (valid >= kBN) {
+#pragma unroll
+        for (int i = 0; i < 128; ++i) mx = fmaxf(mx, __uint_as_float(sr[i]));
+      } else {
+#pragma unroll
+        for (int i = 0; i < 128; ++i)
+          if (i < valid) mx = fmaxf(mx, __uint_as_float(sr[i]));
+      }
+      const float m_new = mx * sl2;
+      if (m_new > m_used + kRescaleThreshold) {
+        const float alpha = ex2_approx(m_used - m_new);  // 0 on the first block
+        if (j > 0) {
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld_x32(tO + c * 32, o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st_x32(tO + c * 32, o);
+          }
+        }
+        l *= alpha;
+        m_used = m_new;
+      }
+      const float neg_m = -m_used;
+      uint32_t pk[64];
+      float rs0 = 0.f, rs1 = 0.f;
+      if (valid >= kBN) {
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          const float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * i]), sl2, neg_m));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * i + 1]), sl2, neg_m));
+          rs0 += p0;
+          rs1 += p1;
+          pk[i] = pack_bf16x2(p0, p1);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * i]), sl2, neg_m));
+          float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * i + 1]), sl2, neg_m));
+          p0 = (2 * i < valid) ? p0 : 0.f;
+          p1 = (2 * i + 1 < valid) ? p1 : 0.f;
+          rs0 += p0;
+          rs1 += p1;
+          pk[i] = pack_bf16x2(p0, p1);
+        }
+      }
+      l += rs0 + rs1;
+      tmem_st_x64(tS, pk);
+      tc_fence_before();
+      if (!(p.inject_stall && t == 0 && j == 0 && it == 0)) mbar_arrive(BAR(C::PF + t));
+    }
+    // ---- epilogue: the tile owner stores its rows to their destination and moves on
+    const bool got = __all_sync(0xffffffffu, mbar_wait(BAR(C::OF + t), it & 1, w));
+    if (!got) return;
+    tc_fence_after();
+    uint32_t o[D];
+    if constexpr (D == 128) tmem_ld_x128(tO, o);
+    else tmem_ld_x64(tO, o);
+    tc_fence_before();
+    mbar_arrive(BAR(C::OE + t));  // O_t may now be overwritten by the next item
+    if (srow < p.S) {
+      const float inv_l = 1.0f / l;
+      uint16_t* dst = out_row_ptr<D, A2A>(p.epi, p.B, p.H, p.S, wi.b, wi.h, srow);
+      uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+      for (int c = 0; c < D / 8; ++c) {
+        uint4 v;
+        v.x = pack_bf16x2(__uint_as_float(o[8 * c + 0]) * inv_l, __uint_as_float(o[8 * c + 1]) * inv_l);
+        v.y = pack_bf16x2(__uint_as_float(o[8 * c + 2]) * inv_l, __uint_as_float(o[8 * c + 3]) * inv_l);
+        v.z = pack_bf16x2(__uint_as_float(o[8 * c + 4]) * inv_l, __uint_as_float(o[8 * c + 5]) * inv_l);
+        v.w = pack_bf16x2(__uint_as_float(o[8 * c + 6]) * inv_l, __uint_as_float(o[8 * c + 7]) * inv_l);
+        d4[c] = v;
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ kernel
+template <int D, bool A2A>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ Params p) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t* sgen = smem_raw + (sbase - raw);
+  const uint32_t bar0 = sbase + C::BAR_OFF;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sgen + C::MISC_OFF);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sgen + C::MISC_OFF + 4);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+  if (threadIdx.x == 0) {
+    auto BAR = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(BAR(C::QF + t), 1);
+      mbar_init(BAR(C::QE + t), 1);
+      mbar_init(BAR(C::SF + t), 1);
+      mbar_init(BAR(C::PF + t), kBM);
+      mbar_init(BAR(C::OF + t), 1);
+      mbar_init(BAR(C::OE + t), kBM);
+    }
+    for (int s = 0; s < C::NSTAGE; ++s) {
+      mbar_init(BAR(C::KVF + s), 1);
+      mbar_init(BAR(C::KVE + s), 1);
+    }
+    mbar_init(BAR(C::DONE), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtl w{abort_flag, p.dev_status, p.timeout_ns};
+
+  if (warp == 0) {
+    if (lane == 0) producer_role<D>(p, &tmQ, &tmK, &tmV, sbase, bar0, w);
+  } else if (warp == 1) {
+    if (lane == 0) mma_role<D>(p, sbase, bar0, tmem, w);
+  } else if (warp >= 4) {
+    softmax_role<D, A2A>(p, (warp - 4) / 4, bar0, tmem, w);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace tc
+}  // namespace attn_a2a

@@ -1,0 +1,31 @@
+// Host-side glue shared by the translation units of libattn_a2a.so.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "../../include/attn_a2a.h"
+#include "epilogue.cuh"
+
+namespace attn_a2a {
+
+// Validated problem description handed to the launchers.
+struct Problem {
+  int B, H, S, d;
+  float scale;
+};
+
+int num_sms_current_device();
+
+int launch_fa_tc(const void* q, const void* k, const void* v, const attn_a2a_shape& shp,
+                 float scale, bool a2a, const EpiParams& epi, int* dev_status,
+                 const attn_a2a_opts& opts, cudaStream_t stream);
+
+int launch_fa_simt(const void* q, const void* k, const void* v, const attn_a2a_shape& shp,
+                   float scale, const EpiParams& epi, cudaStream_t stream);
+
+int launch_permute(const void* o, const attn_a2a_shape& shp, const EpiParams& epi,
+                   cudaStream_t stream);
+
+int launch_probe(const xstage_probe_cfg& cfg, cudaStream_t stream);
+
+}  // namespace attn_a2a

@@ -1,0 +1,95 @@
+// Burst-Gap probe (X-Stage pages, Technical Summary, "Methodology": the
+// Burst-Gap model T_iss(G; K, V) = max(T0_iss(K, V), V/R - G) and its measured
+// quantities T0_iss, R and Q; "Key Contributions": characterisation through
+// parameterised microbenchmarks).
+//
+// K producer CTAs repeat: issue a burst of V/K bytes of stores (the shape of
+// the attention epilogue's output rows: 16-byte vector stores, or bulk
+// asynchronous copies from shared memory), then spend a gap G not storing.
+// Thread 0 of each producer stamps %globaltimer at burst start, after the
+// last store of the burst has been issued by every thread of the CTA, and at
+// gap end. Stores are never waited for inside a round: the issuer only sees
+// the time it took to get them accepted, which is what the model predicts.
+#include <cstdint>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace attn_a2a {
+namespace {
+
+constexpr int kProbeThreads = 512;
+constexpr int kBulkChunk = 32768;  // bytes of the shared-memory source of each bulk copy
+
+__global__ void __launch_bounds__(kProbeThreads)
+    xstage_probe_kernel(uint8_t* __restrict__ dst, long long dst_bytes, long long V, int rounds,
+                        long long G_ns, int store_kind, int gap_kind, long long fma_iters,
+                        long long* __restrict__ stamps) {
+  extern __shared__ __align__(128) uint8_t bulk_src[];
+  const int K = gridDim.x, prod = blockIdx.x;
+  const long long share = V / K;
+  const long long nslots = dst_bytes / V;
+  if (store_kind == 1) {
+    for (int i = threadIdx.x; i < kBulkChunk / 4; i += blockDim.x)
+      reinterpret_cast<uint32_t*>(bulk_src)[i] = 0x3c003c00u ^ static_cast<uint32_t>(i);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  float acc = 1.0f + 1e-3f * threadIdx.x;
+  uint64_t t0 = 0, t1 = 0, t2 = 0;
+  for (int r = 0; r < rounds; ++r) {
+    __syncthreads();
+    if (threadIdx.x == 0) t0 = globaltimer_ns();
+    uint8_t* base = dst + (r % nslots) * V + prod * share;
+    if (store_kind == 0) {
+      const uint4 val = make_uint4(static_cast<uint32_t>(r), static_cast<uint32_t>(prod), threadIdx.x, 0u);
+      uint4* b4 = reinterpret_cast<uint4*>(base);
+      const long long n = share / 16;
+      for (long long i = threadIdx.x; i < n; i += blockDim.x) b4[i] = val;
+    } else if (threadIdx.x == 0) {
+      const uint32_t src = smem_u32(bulk_src);
+      for (long long off = 0; off < share; off += kBulkChunk) {
+        const long long left = share - off;
+        const uint32_t size = static_cast<uint32_t>(left < kBulkChunk ? left : kBulkChunk);
+        asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(base + off),
+                     "r"(src), "r"(size)
+                     : "memory");
+      }
+      asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) t1 = globaltimer_ns();
+    if (gap_kind == 0) {
+      if (threadIdx.x == 0)
+        while (globaltimer_ns() - t1 < static_cast<uint64_t>(G_ns)) {
+        }
+    } else {
+      for (long long i = 0; i < fma_iters; ++i) acc = fmaf(acc, 0.99999988f, 1.1920929e-7f);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      t2 = globaltimer_ns();
+      long long* st = stamps + (static_cast<long long>(prod) * rounds + r) * 3;
+      st[0] = static_cast<long long>(t0);
+      st[1] = static_cast<long long>(t1);
+      st[2] = static_cast<long long>(t2);
+    }
+  }
+  if (store_kind == 1 && threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+  if (acc == 1234.5f) dst[0] = 1;  // keeps the gap's FMA chain from being removed
+}
+
+}  // namespace
+
+int launch_probe(const xstage_probe_cfg& c, cudaStream_t stream) {
+  const int smem = c.store_kind == 1 ? kBulkChunk : 0;
+  if (smem > 0 &&
+      cudaFuncSetAttribute(xstage_probe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+          cudaSuccess)
+    return ATTN_A2A_ECUDA;
+  xstage_probe_kernel<<<c.K, kProbeThreads, smem, stream>>>(
+      static_cast<uint8_t*>(c.dst), c.dst_bytes, c.V_bytes, c.rounds, c.G_ns, c.store_kind,
+      c.gap_kind, c.fma_iters, c.stamps);
+  return cudaGetLastError() == cudaSuccess ? ATTN_A2A_OK : ATTN_A2A_ECUDA;
+}
+
+}  // namespace attn_a2a

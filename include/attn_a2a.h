@@ -1,0 +1,196 @@
+/*
+ * attn_a2a.h - C ABI of libattn_a2a.so: non-causal bf16 attention forward on
+ * NVIDIA GB300 (sm_103a) fused with the post-attention Ulysses all-to-all
+ * layout change, plus a Burst-Gap store probe.
+ *
+ * Source of the operations (X-Stage: An Overlooked Pipeline Stage for
+ * Communication-Computation Overlap in DiT Inference, gist.science
+ * explanation):
+ *   - "Key Contributions", FlashAttention-A2A (piggybacking): in Ulysses
+ *     sequence-parallel attention the post-attention all-to-all is fused into
+ *     FlashAttention; the owner of each output tile issues the stores of that
+ *     tile to its destination and resumes the Q loop of its next tile, with no
+ *     dedicated communication warp or SM.
+ *   - Technical Summary, "Methodology", Burst-Gap equation
+ *     T_iss(G; K, V) = max(T0_iss(K, V), V/R - G) with the measured
+ *     quantities T0_iss, R and Q.
+ *
+ * Shapes and layouts (all tensors bf16, element strides in ELEMENTS):
+ *   q, k, v : logical [B, H, S, d], innermost d contiguous; the caller gives
+ *             the batch, head and sequence strides. "Head-sharded": virtual
+ *             rank r holds heads [r*H/P, (r+1)*H/P) over the full sequence.
+ *   output  : P partitions, partition j is a contiguous [B, c_j, H, d] array
+ *             holding sequence rows [start_j, start_j + c_j) of every head
+ *             ("sequence-sharded"). c_j = floor(S/P) + (j < S mod P ? 1 : 0),
+ *             start_j = sum of the earlier c_i (torch.tensor_split rule).
+ *   math    : O[b,h] = softmax(scale * Q[b,h] K[b,h]^T) V[b,h]; fp32
+ *             accumulation, probabilities rounded to bf16 before the P*V
+ *             product, output rounded to bf16 (round to nearest even).
+ *
+ * Conventions shared by every entry point:
+ *   - Ownership: the caller owns every buffer. The library allocates no
+ *     device memory; it keeps small host-side state only (a cached driver
+ *     entry point and the SM count per device).
+ *   - Streams: `stream` is a cudaStream_t passed as void* (NULL = the legacy
+ *     default stream). Work is asynchronous on that stream.
+ *   - Errors: argument errors are detected on the host and returned
+ *     synchronously before anything is launched (ATTN_A2A_EINVAL /
+ *     ATTN_A2A_EUNSUPPORTED). A launch failure returns ATTN_A2A_ECUDA.
+ *     Every in-kernel wait is bounded; if one expires the kernel stops all of
+ *     its roles, writes ATTN_A2A_ETIMEOUT to *dev_status (when dev_status is
+ *     not NULL) and returns, leaving the context usable. dev_status is a
+ *     device int the caller clears to 0 beforehand and reads when it wants.
+ *   - Alignment: every pointer 16-byte aligned; batch, head and sequence
+ *     strides multiples of 8 elements (16 bytes).
+ *   - Outputs must not alias inputs.
+ */
+#ifndef ATTN_A2A_H
+#define ATTN_A2A_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ATTN_A2A_OK = 0,
+  ATTN_A2A_EINVAL = 1,        /* bad argument (null, misaligned, out of range) */
+  ATTN_A2A_EUNSUPPORTED = 2,  /* valid but not built (e.g. d not in {64,128}) */
+  ATTN_A2A_ECUDA = 3,         /* CUDA runtime/driver error at launch */
+  ATTN_A2A_ETIMEOUT = 4       /* a bounded in-kernel wait expired (device status) */
+} attn_a2a_status;
+
+/* Problem shape and input strides (elements). d is contiguous. */
+typedef struct {
+  int B, H, S, d;
+  long long q_sb, q_sh, q_ss;
+  long long k_sb, k_sh, k_ss;
+  long long v_sb, v_sh, v_ss;
+} attn_a2a_shape;
+
+/* Tuning and test options for the *_ex entry points. Zero-initialised means
+ * the defaults used by the plain entry points. */
+typedef struct {
+  int store_kind;       /* 0: vector st.global of each owned output row straight from
+                           registers; 1: rows staged in shared memory and sent with
+                           asynchronous bulk copies (cp.async.bulk), the issuing thread
+                           waiting only until its staging row has been read */
+  int grid;             /* persistent CTAs; 0 = one per SM */
+  long long timeout_ns; /* limit of every in-kernel wait; 0 = 2 000 000 000 ns */
+  int inject_stall;     /* test hook, 0 in normal use. 1 = the softmax role of the first
+                           query tile withholds its first "probabilities ready" signal,
+                           so the MMA role's bounded wait expires and the kernel reports
+                           ATTN_A2A_ETIMEOUT through dev_status and exits cleanly */
+  int reserved[3];
+} attn_a2a_opts;
+
+/*
+ * attn_a2a_fwd - fused attention + head-to-sequence all-to-all (the product).
+ * The owner of each 128-row output tile of head h stores row s of that tile
+ * to out_partitions[j][b, s - start_j, h, :] where j is the chunk holding s,
+ * then returns to its next tile. A tile that straddles a chunk boundary is
+ * split row by row; rows >= S are never stored.
+ *   q, k, v        : device bf16, layout above, caller-owned, read only.
+ *   shp            : host pointer to the shape/strides.
+ *   P              : virtual ranks, 1 <= P <= 64, H % P == 0.
+ *   scale          : softmax scale, finite and >= 0 (1/sqrt(d) in DiT).
+ *   out_partitions : HOST array of P device pointers, partition j is
+ *                    [B, c_j, H, d] bf16 contiguous (may be NULL if c_j == 0).
+ *   dev_status     : optional device int (NULL allowed), see conventions.
+ * Returns an attn_a2a_status.
+ */
+int attn_a2a_fwd(const void* q, const void* k, const void* v, const attn_a2a_shape* shp,
+                 int P, float scale, void* const* out_partitions, int* dev_status,
+                 void* stream);
+
+/* attn_a2a_fwd with options (NULL opts = defaults). */
+int attn_a2a_fwd_ex(const void* q, const void* k, const void* v, const attn_a2a_shape* shp,
+                    int P, float scale, void* const* out_partitions, int* dev_status,
+                    const attn_a2a_opts* opts, void* stream);
+
+/*
+ * attn_a2a_fwd_contig - "attention alone": the same kernel and arithmetic
+ * with the output tile stored contiguously to out = [B, H, S, d] bf16
+ * (device, contiguous). Followed by attn_a2a_permute it is the serial
+ * baseline (attention, then a separate all-to-all) of the pages' Results,
+ * FlashAttention-A2A optimisation; its output is bit-identical to the fused
+ * path's after the permutation.
+ */
+int attn_a2a_fwd_contig(const void* q, const void* k, const void* v, const attn_a2a_shape* shp,
+                        float scale, void* out, int* dev_status, void* stream);
+
+int attn_a2a_fwd_contig_ex(const void* q, const void* k, const void* v,
+                           const attn_a2a_shape* shp, float scale, void* out, int* dev_status,
+                           const attn_a2a_opts* opts, void* stream);
+
+/*
+ * attn_a2a_permute - the serial all-to-all on its own: a pure copy of a
+ * contiguous [B, H, S, d] bf16 device tensor o into the P partitions
+ * (same layout and chunk rule as attn_a2a_fwd). shp supplies B, H, S, d; its
+ * strides are ignored. H % P == 0 is required as for the fused call.
+ */
+int attn_a2a_permute(const void* o, const attn_a2a_shape* shp, int P,
+                     void* const* out_partitions, void* stream);
+
+/*
+ * attn_a2a_fwd_simt - slow SIMT debug path (no tensor cores): the same
+ * attention and the same partition epilogue computed by one warp per query
+ * row in fp32 (probabilities are not rounded to bf16). For bring-up and
+ * cross-checks on small problems only.
+ */
+int attn_a2a_fwd_simt(const void* q, const void* k, const void* v, const attn_a2a_shape* shp,
+                      int P, float scale, void* const* out_partitions, void* stream);
+
+/*
+ * attn_a2a_fwd_host - the product call from host memory, for callers whose
+ * data lives on the host. On `stream`: copies q, k, v (host, contiguous
+ * [B,H,S,d] bf16, pinned for asynchronous copies) into the caller's device
+ * buffers dq, dk, dv, runs attn_a2a_fwd into the caller's device partitions
+ * dparts[j], then copies each partition back into hparts[j] (host). Returns
+ * after enqueueing; synchronise the stream before reading hparts.
+ */
+int attn_a2a_fwd_host(const void* hq, const void* hk, const void* hv, const attn_a2a_shape* shp,
+                      int P, float scale, void* dq, void* dk, void* dv,
+                      void* const* dparts, void* const* hparts, int* dev_status, void* stream);
+
+/*
+ * Burst-Gap probe (Technical Summary, "Methodology"; "Key Contributions",
+ * characterisation by parameterised microbenchmarks). K producer CTAs run
+ * `rounds` rounds; in each round every producer issues its share V/K of an
+ * aggregate store burst of V bytes, then computes for a gap of G ns. Each
+ * producer records three %globaltimer stamps per round into
+ * stamps[(p * rounds + r) * 3 + {0,1,2}]: burst start, last store issued,
+ * gap end. The issuer-visible issue time is stamp1 - stamp0. Destinations
+ * advance through dst (dst_bytes, device, caller-owned scratch) so that
+ * successive bursts do not hit the same lines; make dst_bytes several times
+ * the L2 size to measure drain into HBM.
+ */
+typedef struct {
+  int K;                 /* producer CTAs, 1 .. 1024 */
+  int rounds;            /* rounds per producer, >= 1 */
+  long long V_bytes;     /* aggregate burst volume per round; multiple of 4096*K */
+  long long G_ns;        /* gap after each burst, ns, >= 0 */
+  int store_kind;        /* 0: st.global.v4 by all producer threads;
+                            1: cp.async.bulk from shared memory, issued by one thread */
+  int gap_kind;          /* 0: spin on %globaltimer for G_ns (the issuer stays idle);
+                            1: dependent FMA chain on every producer thread sized by the
+                               host to last about G_ns (the issuer computes) */
+  void* dst;             /* device scratch target, 16-byte aligned */
+  long long dst_bytes;   /* >= V_bytes, multiple of 4096*K */
+  long long* stamps;     /* device int64 [K][rounds][3] */
+  long long fma_iters;   /* gap_kind 1: dependent FMAs per thread per gap (host-calibrated) */
+} xstage_probe_cfg;
+
+int xstage_probe_run(const xstage_probe_cfg* cfg, void* stream);
+
+/* Static description of a status code. Never NULL. */
+const char* attn_a2a_strerror(int status);
+
+/* Number of SMs the library sizes its persistent grid to on the current device
+ * (0 if no device). Host-only query, no launch. */
+int attn_a2a_num_sms(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_A2A_H */

@@ -1,0 +1,135 @@
+"""CPU tests of the C ABI: the library builds, loads and exports every symbol
+the header declares; host-side argument validation rejects bad calls with
+the documented status before any CUDA call (the pointers used here are fake
+and never dereferenced)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from attention_all_layout_gb300 import binding as bd
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn_a2a.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(bd.LIB_PATH):
+        from attention_all_layout_gb300 import build
+
+        build.build()
+    return bd.load()
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\**(\w+)\s*\(", text, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "return")))
+
+
+def test_header_declares_expected_entry_points():
+    assert header_functions() == sorted(bd.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in header_functions():
+        assert hasattr(lib, name), name
+
+
+def test_strerror(lib):
+    assert bd.strerror(bd.OK) == "ok"
+    assert "invalid" in bd.strerror(bd.EINVAL)
+    assert "wait" in bd.strerror(bd.ETIMEOUT)
+    assert bd.strerror(99) == "unknown status"
+
+
+FAKE = 1 << 20  # 16-byte aligned, never dereferenced
+
+
+def call_fwd(lib, B=1, H=4, S=256, d=64, P=2, scale=0.125, q=FAKE, k=FAKE * 2, v=FAKE * 3, parts=None,
+             strides=None, opts=None):
+    sb, sh, ss = H * S * d, S * d, d
+    st = strides or (sb, sh, ss)
+    shp = bd.Shape(B, H, S, d, *st, *st, *st)
+    if parts is None:
+        parts = [FAKE * (16 + j) for j in range(max(P, 1))]
+    arr = (ctypes.c_void_p * max(1, len(parts)))(*parts)
+    o = ctypes.byref(opts) if opts is not None else None
+    return lib.attn_a2a_fwd_ex(q, k, v, ctypes.byref(shp), P, scale, arr, None, o, None)
+
+
+@pytest.mark.parametrize(
+    "kw,code",
+    [
+        (dict(P=0), bd.EINVAL),
+        (dict(P=65, H=65), bd.EINVAL),
+        (dict(P=3, H=4), bd.EINVAL),  # H % P != 0
+        (dict(d=96), bd.EUNSUPPORTED),
+        (dict(d=0), bd.EINVAL),
+        (dict(scale=-1.0), bd.EINVAL),
+        (dict(scale=float("nan")), bd.EINVAL),
+        (dict(scale=float("inf")), bd.EINVAL),
+        (dict(q=0), bd.EINVAL),
+        (dict(k=FAKE + 8), bd.EINVAL),  # misaligned
+        (dict(parts=[FAKE * 16, 0]), bd.EINVAL),  # null partition with rows
+        (dict(parts=[FAKE * 16, FAKE * 17 + 2]), bd.EINVAL),  # misaligned partition
+        (dict(strides=(4 * 256 * 64, 256 * 64, 60)), bd.EINVAL),  # sequence stride not a multiple of 8
+        (dict(strides=(4 * 256 * 64, -256 * 64, 64)), bd.EINVAL),
+        (dict(B=-1), bd.EINVAL),
+        (dict(parts=[FAKE * 2, FAKE * 40]), bd.EINVAL),  # partition 0 aliases k
+    ],
+)
+def test_fwd_rejects_bad_arguments(lib, kw, code):
+    assert call_fwd(lib, **kw) == code
+
+
+def test_bad_options_rejected(lib):
+    assert call_fwd(lib, opts=bd._opts(store_kind=7)) == bd.EINVAL
+    assert call_fwd(lib, opts=bd._opts(grid=-1)) == bd.EINVAL
+    assert call_fwd(lib, opts=bd._opts(timeout_ns=-5)) == bd.EINVAL
+
+
+def test_empty_problem_is_ok_without_launch(lib):
+    # S = 0: every chunk is empty, null partitions are allowed, nothing is launched
+    assert call_fwd(lib, S=0, parts=[0, 0]) == bd.OK
+    assert call_fwd(lib, B=0, parts=[0, 0]) == bd.OK
+
+
+def test_contig_and_permute_validation(lib):
+    shp = bd.plain_shape(1, 4, 256, 64)
+    assert lib.attn_a2a_fwd_contig(FAKE, FAKE * 2, FAKE * 3, ctypes.byref(shp), 0.1, None, None, None) == bd.EINVAL
+    # output overlapping q
+    assert lib.attn_a2a_fwd_contig(FAKE, FAKE * 4, FAKE * 8, ctypes.byref(shp), 0.1, FAKE + 64, None, None) == bd.EINVAL
+    parts = (ctypes.c_void_p * 2)(FAKE * 16, FAKE * 17)
+    assert lib.attn_a2a_permute(None, ctypes.byref(shp), 2, parts, None) == bd.EINVAL
+    assert lib.attn_a2a_permute(FAKE, ctypes.byref(shp), 3, parts, None) == bd.EINVAL
+    bad = bd.plain_shape(1, 4, 256, 80)
+    assert lib.attn_a2a_permute(FAKE, ctypes.byref(bad), 2, parts, None) == bd.EUNSUPPORTED
+
+
+def test_probe_validation(lib):
+    def run(**kw):
+        c = dict(K=4, rounds=3, V_bytes=4096 * 4, G_ns=0, store_kind=0, gap_kind=0, dst=FAKE,
+                 dst_bytes=4096 * 16, stamps=FAKE, fma_iters=0)
+        c.update(kw)
+        cfg = bd.ProbeCfg(c["K"], c["rounds"], c["V_bytes"], c["G_ns"], c["store_kind"], c["gap_kind"],
+                          c["dst"], c["dst_bytes"], c["stamps"], c["fma_iters"])
+        return lib.xstage_probe_run(ctypes.byref(cfg), None)
+
+    assert run(K=0) == bd.EINVAL
+    assert run(rounds=0) == bd.EINVAL
+    assert run(V_bytes=4096 * 4 + 16) == bd.EINVAL
+    assert run(dst_bytes=4096) == bd.EINVAL
+    assert run(store_kind=2) == bd.EINVAL
+    assert run(G_ns=-1) == bd.EINVAL
+    assert run(stamps=0) == bd.EINVAL
+    assert run(dst=FAKE + 4) == bd.EINVAL
+
+
+def test_chunk_sizes_rule():
+    assert bd.chunk_sizes(75600, 8) == [9450] * 8
+    assert bd.chunk_sizes(10, 4) == [3, 3, 2, 2]
+    assert bd.chunk_sizes(3, 8) == [1, 1, 1, 0, 0, 0, 0, 0]

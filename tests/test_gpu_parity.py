@@ -1,0 +1,171 @@
+"""GPU parity: the fused tcgen05 kernel (through the C ABI) against the
+float64 oracle, the partition layout bit-exact against attention-then-permute
+on the GPU, guard bands intact, ragged and degenerate shapes, strided
+inputs, the host-memory entry point, and the bounded-wait failure path."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from attention_all_layout_gb300 import binding as bd
+from attention_all_layout_gb300 import workloads
+from oracle import attention as orc
+
+from gpu_helpers import GuardedPartitions, compare, fused, partitions_to_bhsd
+
+pytestmark = pytest.mark.gpu
+
+
+def cuda_qkv(cfg, seed=0):
+    q, k, v = workloads.make_qkv(cfg, seed=seed)
+    return q, k, v, q.cuda(), k.cuda(), v.cuda()
+
+
+# (name, B, H, S, d, P): the small presets run in full against the oracle,
+# plus ragged shapes that span several tiles and end in a partial tile,
+# chunks that straddle tiles, and degenerate sizes.
+FULL_CASES = [
+    ("tiny", 1, 4, 256, 64, 2),
+    ("image", 1, 24, 4096, 128, 4),
+    ("joint", 1, 24, 4608, 128, 8),
+    ("ragged_200_P2", 1, 2, 200, 128, 2),
+    ("ragged_300_P3", 1, 3, 300, 128, 3),
+    ("ragged_1000_P8_d64", 1, 8, 1000, 64, 8),
+    ("ragged_4608_P8_H8", 1, 8, 4608, 128, 8),
+    ("batch2_odd_blocks", 2, 2, 640, 128, 2),
+    ("one_row", 1, 1, 1, 128, 1),
+    ("S_lt_P", 1, 8, 5, 64, 8),
+    ("one_tile_plus_one", 1, 1, 129, 64, 1),
+]
+
+
+def case_cfg(name, B, H, S, d, P):
+    if name in workloads.CONFIGS:
+        return workloads.CONFIGS[name]
+    return workloads.AttnConfig(name, B=B, H=H, S=S, d=d, P=P)
+
+
+@pytest.mark.parametrize("case", FULL_CASES, ids=[c[0] for c in FULL_CASES])
+def test_fused_matches_oracle(case):
+    cfg = case_cfg(*case)
+    q, k, v, dq, dk, dv = cuda_qkv(cfg)
+    g = fused(dq, dk, dv, cfg.P, cfg.scale)
+    assert g.guards_intact(), "epilogue wrote outside a partition"
+    want = orc.head_to_seq_partitions(orc.attention_fp64(q, k, v, cfg.scale), cfg.P)
+    for j, (got, w) in enumerate(zip(g.parts, want)):
+        compare(orc.as_f64(got), w, f"{cfg.name} partition {j}")
+    # per head, so that one wrong head cannot hide in the global norm
+    o = partitions_to_bhsd(g.parts)
+    ref = orc.seq_to_head(want)
+    for h in range(cfg.H):
+        compare(o[:, h], ref[:, h], f"{cfg.name} head {h}")
+
+
+@pytest.mark.parametrize("case", FULL_CASES[:7], ids=[c[0] for c in FULL_CASES[:7]])
+def test_layout_bit_exact_vs_attention_then_permute(case):
+    cfg = case_cfg(*case)
+    _, _, _, dq, dk, dv = cuda_qkv(cfg, seed=1)
+    g = fused(dq, dk, dv, cfg.P, cfg.scale)
+    o = torch.empty((cfg.B, cfg.H, cfg.S, cfg.d), dtype=torch.bfloat16, device="cuda")
+    bd.attn_a2a_fwd_contig(dq, dk, dv, cfg.scale, o)
+    serial = GuardedPartitions(cfg.B, cfg.S, cfg.H, cfg.d, cfg.P)
+    bd.attn_a2a_permute(o, cfg.P, serial.parts)
+    torch.cuda.synchronize()
+    assert serial.guards_intact()
+    for a, b in zip(g.parts, serial.parts):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_contig_matches_oracle():
+    cfg = workloads.config("image", H=4, S=1000)
+    q, k, v, dq, dk, dv = cuda_qkv(cfg, seed=2)
+    o = torch.empty((cfg.B, cfg.H, cfg.S, cfg.d), dtype=torch.bfloat16, device="cuda")
+    bd.attn_a2a_fwd_contig(dq, dk, dv, cfg.scale, o)
+    torch.cuda.synchronize()
+    compare(orc.as_f64(o), orc.attention_fp64(q, k, v, cfg.scale), "contig")
+
+
+def test_simt_debug_path_matches_oracle():
+    cfg = workloads.CONFIGS["tiny"]
+    q, k, v, dq, dk, dv = cuda_qkv(cfg)
+    g = GuardedPartitions(cfg.B, cfg.S, cfg.H, cfg.d, cfg.P)
+    bd.attn_a2a_fwd_simt(dq, dk, dv, cfg.P, cfg.scale, g.parts)
+    torch.cuda.synchronize()
+    assert g.guards_intact()
+    want = orc.head_to_seq_partitions(orc.attention_fp64(q, k, v, cfg.scale), cfg.P)
+    for got, w in zip(g.parts, want):
+        compare(orc.as_f64(got), w, "simt")
+
+
+def test_strided_inputs():
+    # q, k, v are views of [B, S, H, d] buffers (sequence-major memory), as a
+    # Ulysses pre-attention exchange would leave them.
+    B, H, S, d, P = 1, 4, 700, 128, 2
+    gen = torch.Generator().manual_seed(3)
+    base = [torch.randn((B, S, H, d), generator=gen).to(torch.bfloat16) for _ in range(3)]
+    q, k, v = (t.permute(0, 2, 1, 3) for t in base)
+    dq, dk, dv = (t.cuda().permute(0, 2, 1, 3) for t in base)
+    assert dq.stride(2) == H * d
+    scale = 1 / math.sqrt(d)
+    g = fused(dq, dk, dv, P, scale)
+    want = orc.head_to_seq_partitions(orc.attention_fp64(q, k, v, scale), P)
+    for got, w in zip(g.parts, want):
+        compare(orc.as_f64(got), w, "strided")
+
+
+def test_scale_zero_and_constant_v():
+    B, H, S, d, P = 1, 2, 333, 64, 2
+    gen = torch.Generator().manual_seed(4)
+    q = torch.randn((B, H, S, d), generator=gen).to(torch.bfloat16).cuda()
+    k = torch.randn((B, H, S, d), generator=gen).to(torch.bfloat16).cuda()
+    v = torch.randn((B, H, S, d), generator=gen).to(torch.bfloat16).cuda()
+    g = fused(q, k, v, P, 0.0)  # uniform weights: every row is the mean of V
+    got = partitions_to_bhsd(g.parts)
+    mean = orc.as_f64(v).mean(axis=2, keepdims=True)
+    compare(got, np.broadcast_to(mean, got.shape), "scale 0")
+    vc = torch.full_like(v, 0.75)
+    g = fused(q, k, vc, P, 1.0)
+    assert torch.all(torch.cat([p.flatten() for p in g.parts]) == 0.75)
+
+
+def test_empty_sequence_launches_nothing():
+    q = torch.empty((1, 2, 0, 128), dtype=torch.bfloat16, device="cuda")
+    assert bd.attn_a2a_fwd(q, q, q, 2, 0.1, [None, None]) == bd.OK
+
+
+def test_host_entry_point_matches_device_path():
+    cfg = workloads.config("image", H=4, S=1500)
+    q, k, v = workloads.make_qkv(cfg, seed=5)
+    hq, hk, hv = (t.pin_memory() for t in (q, k, v))
+    dq, dk, dv = (torch.empty_like(t, device="cuda") for t in (q, k, v))
+    dparts = bd.alloc_partitions(cfg.B, cfg.S, cfg.H, cfg.d, cfg.P)
+    hparts = [torch.empty_like(p, device="cpu").pin_memory() for p in dparts]
+    bd.attn_a2a_fwd_host(hq, hk, hv, cfg.P, cfg.scale, dq, dk, dv, dparts, hparts)
+    torch.cuda.synchronize()
+    ref = fused(q.cuda(), k.cuda(), v.cuda(), cfg.P, cfg.scale)
+    for a, b in zip(hparts, ref.parts):
+        assert torch.equal(a.view(torch.int16), b.cpu().view(torch.int16))
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    cfg = workloads.CONFIGS["tiny"]
+    _, _, _, dq, dk, dv = cuda_qkv(cfg)
+    parts = bd.alloc_partitions(cfg.B, cfg.S, cfg.H, cfg.d, cfg.P)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    bd.attn_a2a_fwd(dq, dk, dv, cfg.P, cfg.scale, parts, dev_status=status, inject_stall=1,
+                    timeout_ns=50_000_000)
+    torch.cuda.synchronize()
+    assert int(status.item()) == bd.ETIMEOUT
+    # the context is still usable and a normal call is correct afterwards
+    g = fused(dq, dk, dv, cfg.P, cfg.scale)
+    assert g.guards_intact()
+
+
+def test_grid_size_does_not_change_result():
+    cfg = workloads.config("image", H=6, S=1111)
+    _, _, _, dq, dk, dv = cuda_qkv(cfg, seed=6)
+    a = fused(dq, dk, dv, 2, cfg.scale)
+    b = fused(dq, dk, dv, 2, cfg.scale, grid=3)
+    for x, y in zip(a.parts, b.parts):
+        assert torch.equal(x.view(torch.int16), y.view(torch.int16))

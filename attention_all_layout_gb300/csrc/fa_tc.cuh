@@ -230,6 +230,49 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Row maximum of the 128 scores (keys >= valid excluded when MASK).
+template <bool MASK>
+__device__ __forceinline__ float row_max(const uint32_t (&sr)[128], int valid) {
+  float a[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+  for (int i = 0; i < 128; i += 2) {
+    float x0 = __uint_as_float(sr[i]), x1 = __uint_as_float(sr[i + 1]);
+    if (MASK) {
+      x0 = i < valid ? x0 : -INFINITY;
+      x1 = i + 1 < valid ? x1 : -INFINITY;
+    }
+    a[(i / 2) & 3] = max3f(a[(i / 2) & 3], x0, x1);
+  }
+  return max3f(a[0], a[1], fmaxf(a[2], a[3]));
+}
+
+// p_i = 2^(s_i * sl2 - m) for the 128 keys, packed to bf16 pairs in pk;
+// returns the fp32 sum of the p_i. Keys >= valid get p = 0 when MASK.
+template <bool MASK>
+__device__ __forceinline__ float probs(const uint32_t (&sr)[128], uint32_t (&pk)[64], float sl2, float neg_m,
+                                       int valid) {
+  const uint64_t scale2 = f2_pack(sl2, sl2);
+  const uint64_t bias2 = f2_pack(neg_m, neg_m);
+  uint64_t acc[4];
+#pragma unroll
+  for (int a = 0; a < 4; ++a) acc[a] = f2_pack(0.f, 0.f);
+#pragma unroll
+  for (int i = 0; i < 64; ++i) {
+    float x0, x1;
+    f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1])), scale2, bias2), x0, x1);
+    float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+    if (MASK) {
+      p0 = 2 * i < valid ? p0 : 0.f;
+      p1 = 2 * i + 1 < valid ? p1 : 0.f;
+    }
+    acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
+    pk[i] = pack_bf16x2(p0, p1);
+  }
+  float s0, s1;
+  f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), s0, s1);
+  return s0 + s1;
+}
+
 template <int D, bool A2A>
 __device__ void softmax_role(const Params& p, int t, uint32_t bar0, uint32_t tmem, const WaitCtl& w) {
   using C = Cfg<D>;
@@ -255,56 +298,32 @@ __device__ void softmax_role(const Params& p, int t, uint32_t bar0, uint32_t tme
       uint32_t sr[128];
       tmem_ld_x128(tS, sr);
       const int valid = p.S - j * kBN;  // keys of this block that exist (>= 128 except at the end)
-      float mx = -INFINITY;
-      if (valid >= kBN) {
-#pragma unroll
-        for (int i = 0; i < 128; ++i) mx = fmaxf(mx, __uint_as_float(sr[i]));
-      } else {
-#pragma unroll
-        for (int i = 0; i < 128; ++i)
-          if (i < valid) mx = fmaxf(mx, __uint_as_float(sr[i]));
-      }
+      const float mx = valid >= kBN ? row_max<false>(sr, valid) : row_max<true>(sr, valid);
       const float m_new = mx * sl2;
       if (m_new > m_used + kRescaleThreshold) {
         const float alpha = ex2_approx(m_used - m_new);  // 0 on the first block
         if (j > 0) {
+          const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
             uint32_t o[32];
             tmem_ld_x32(tO + c * 32, o);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            for (int i = 0; i < 32; i += 2) {
+              float x0, x1;
+              f2_unpack(f2_mul(f2_pack(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), a2), x0, x1);
+              o[i] = __float_as_uint(x0);
+              o[i + 1] = __float_as_uint(x1);
+            }
             tmem_st_x32(tO + c * 32, o);
           }
         }
         l *= alpha;
         m_used = m_new;
       }
-      const float neg_m = -m_used;
       uint32_t pk[64];
-      float rs0 = 0.f, rs1 = 0.f;
-      if (valid >= kBN) {
-#pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          const float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * i]), sl2, neg_m));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * i + 1]), sl2, neg_m));
-          rs0 += p0;
-          rs1 += p1;
-          pk[i] = pack_bf16x2(p0, p1);
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * i]), sl2, neg_m));
-          float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * i + 1]), sl2, neg_m));
-          p0 = (2 * i < valid) ? p0 : 0.f;
-          p1 = (2 * i + 1 < valid) ? p1 : 0.f;
-          rs0 += p0;
-          rs1 += p1;
-          pk[i] = pack_bf16x2(p0, p1);
-        }
-      }
-      l += rs0 + rs1;
+      l += valid >= kBN ? probs<false>(sr, pk, sl2, -m_used, valid)
+                        : probs<true>(sr, pk, sl2, -m_used, valid);
       tmem_st_x64(tS, pk);
       tc_fence_before();
       if (!(p.inject_stall && t == 0 && j == 0 && it == 0)) mbar_arrive(BAR(C::PF + t));

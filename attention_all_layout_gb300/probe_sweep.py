@@ -1,0 +1,115 @@
+"""Burst-Gap sweep on the current GPU: runs the probe over a (V, G, K, store
+kind) grid, fits T0_iss, R and Q, and reports the equation's predictions on
+held-out points (X-Stage pages, Technical Summary, "Methodology"; "Key
+Contributions", characterisation and prediction).
+
+Usage: python -m attention_all_layout_gb300.probe_sweep [--quick] [--out FILE]
+The destination of the bursts rotates through a buffer of at least four
+times the L2 size, so that the fitted R is the drain into HBM rather than
+absorption by L2.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import random
+import statistics
+import sys
+
+import torch
+
+from . import binding as bd
+from . import burst_gap as bg
+
+G_US = (0, 0.5, 1, 2, 4, 6, 8, 10, 12, 16, 20)
+V_MB = (1, 2, 4, 8, 16, 32, 64)
+
+
+def round_volume(v_bytes: float, K: int) -> int:
+    unit = 4096 * K
+    return max(unit, int(round(v_bytes / unit)) * unit)
+
+
+class Prober:
+    def __init__(self, dst_bytes: int, max_stamps: int):
+        self.dst = torch.empty(dst_bytes, dtype=torch.uint8, device="cuda")
+        self.stamps = torch.zeros(max_stamps, dtype=torch.int64, device="cuda")
+
+    def run(self, K, V, G_ns, rounds, store_kind=0, gap_kind=0, fma_iters=0, discard=None) -> bg.Point:
+        st = self.stamps[: K * rounds * 3]
+        bd.xstage_probe_run(K, rounds, V, int(G_ns), self.dst, st, store_kind=store_kind, gap_kind=gap_kind,
+                            fma_iters=fma_iters)
+        torch.cuda.synchronize()
+        s = st.view(K, rounds, 3).cpu().tolist()
+        # keep the second half: the queue needs rounds to reach its steady state
+        t_iss, period, first = bg.reduce_stamps(s, discard=rounds // 2 if discard is None else discard)
+        return bg.Point(K=K, V=float(V), G=G_ns * 1e-9, store_kind=store_kind, t_iss=t_iss, period=period,
+                        first=first)
+
+
+def l2_bytes() -> int:
+    return int(torch.cuda.get_device_properties(0).L2_cache_size)
+
+
+def sweep(quick: bool = False, kinds=(0, 1), rounds: int = 64, seed: int = 0) -> dict:
+    K = bd.num_sms()
+    dst_bytes = max(4 * l2_bytes(), 2 * 64 * 2**20)
+    dst_bytes = (dst_bytes // (4096 * K) + 1) * 4096 * K
+    pr = Prober(dst_bytes, 1024 * rounds * 3)
+    gs = G_US if not quick else (0, 1, 4, 10, 20)
+    vs = V_MB if not quick else (2, 16, 64)
+    pr.run(K, round_volume(2**20, K), 0, 5)  # warm-up launch
+    points = []
+    for kind in kinds:
+        for vmb in vs:
+            V = round_volume(vmb * 2**20, K)
+            for g in gs:
+                points.append(pr.run(K, V, g * 1000, rounds, store_kind=kind))
+    # T0 as a function of the producer count, backpressure-free (long gap)
+    t0_k = []
+    for k in (1, 8, 32, K):
+        V = round_volume(8 * 2**20, k)
+        p = pr.run(k, V, 20000, rounds, store_kind=0)
+        t0_k.append({"K": k, "V": V, "t0_us": p.t_iss_med * 1e6})
+    # calibration / held-out split: every third G value is held out
+    rnd = random.Random(seed)
+    held, cal = [], []
+    for p in points:
+        (held if rnd.random() < 0.33 and p.G not in (0.0, max(gs) * 1e-6) else cal).append(p)
+    f = bg.fit(cal)
+    res = bg.residuals(f, held)
+    out = {
+        "K": K,
+        "l2_bytes": l2_bytes(),
+        "dst_bytes": dst_bytes,
+        "rounds": rounds,
+        "fit": {"R_GBps": f.R / 1e9, "Q_MB": None if f.Q is None else f.Q / 2**20,
+                "T0_us": {f"K={k[0]} V={k[1] / 2**20:.2f}MB kind={k[2]}": v * 1e6 for k, v in f.T0.items()}},
+        "heldout": {"n": len(held), "median_abs_rel": statistics.median([abs(r) for r in res]) if res else None,
+                    "max_abs_rel": max((abs(r) for r in res), default=None),
+                    "frac_within_15pct": (sum(abs(r) <= 0.15 for r in res) / len(res)) if res else None},
+        "t0_vs_K": t0_k,
+        "points": [{"V_MB": p.V / 2**20, "G_us": p.G * 1e6, "kind": p.store_kind, "t_iss_us": p.t_iss_med * 1e6,
+                    "period_us": p.period_med * 1e6, "first_us": p.first * 1e6,
+                    "pred_us": f.predict(p) * 1e6 if (p.K, p.V, p.store_kind) in f.T0 else None}
+                   for p in points],
+    }
+    return out
+
+
+def main(argv=None) -> int:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--quick", action="store_true")
+    ap.add_argument("--out", default=None)
+    a = ap.parse_args(argv)
+    res = sweep(quick=a.quick)
+    text = json.dumps(res, indent=1)
+    if a.out:
+        with open(a.out, "w") as fh:
+            fh.write(text)
+    print(json.dumps({k: res[k] for k in ("K", "fit", "heldout", "t0_vs_K")}, indent=1))
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -112,6 +112,7 @@ int fwd_common(const void* q, const void* k, const void* v, const attn_a2a_shape
   if (opts != nullptr && (opts->store_kind < 0 || opts->store_kind > 1 || opts->grid < 0 ||
                           opts->timeout_ns < 0 || opts->inject_stall < 0 || opts->inject_stall > 1))
     return ATTN_A2A_EINVAL;
+  if (opts != nullptr && opts->store_kind != 0) return ATTN_A2A_EUNSUPPORTED;  // bulk epilogue not built
   EpiParams epi;
   std::memset(&epi, 0, sizeof(epi));
   if (a2a) {

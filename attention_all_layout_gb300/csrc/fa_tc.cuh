@@ -300,8 +300,14 @@ __device__ void softmax_role(const Params& p, int t, uint32_t bar0, uint32_t tme
       const int valid = p.S - j * kBN;  // keys of this block that exist (>= 128 except at the end)
       const float mx = valid >= kBN ? row_max<false>(sr, valid) : row_max<true>(sr, valid);
       const float m_new = mx * sl2;
-      if (m_new > m_used + kRescaleThreshold) {
-        const float alpha = ex2_approx(m_used - m_new);  // 0 on the first block
+      // Lazy rescaling: keep a stale row maximum until some row of the warp
+      // has moved more than 2^8 past it. The decision is warp-uniform because
+      // the TMEM loads and stores below are warp-collective; rows whose
+      // maximum did not grow get alpha = 2^0 = 1 exactly.
+      if (__any_sync(0xffffffffu, m_new > m_used + kRescaleThreshold)) {
+        const float m_tgt = fmaxf(m_used, m_new);
+        // 0 on the first block (m_used = -inf); exactly 1 where the maximum did not move
+        const float alpha = m_tgt == m_used ? 1.0f : ex2_approx(m_used - m_tgt);
         if (j > 0) {
           const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll
@@ -319,7 +325,7 @@ __device__ void softmax_role(const Params& p, int t, uint32_t bar0, uint32_t tme
           }
         }
         l *= alpha;
-        m_used = m_new;
+        m_used = m_tgt;
       }
       uint32_t pk[64];
       l += valid >= kBN ? probs<false>(sr, pk, sl2, -m_used, valid)

@@ -71,9 +71,8 @@ typedef struct {
  * the defaults used by the plain entry points. */
 typedef struct {
   int store_kind;       /* 0: vector st.global of each owned output row straight from
-                           registers; 1: rows staged in shared memory and sent with
-                           asynchronous bulk copies (cp.async.bulk), the issuing thread
-                           waiting only until its staging row has been read */
+                           registers (the only epilogue built; any other value returns
+                           ATTN_A2A_EUNSUPPORTED) */
   int grid;             /* persistent CTAs; 0 = one per SM */
   long long timeout_ns; /* limit of every in-kernel wait; 0 = 2 000 000 000 ns */
   int inject_stall;     /* test hook, 0 in normal use. 1 = the softmax role of the first

@@ -88,6 +88,7 @@ def test_fwd_rejects_bad_arguments(lib, kw, code):
 
 def test_bad_options_rejected(lib):
     assert call_fwd(lib, opts=bd._opts(store_kind=7)) == bd.EINVAL
+    assert call_fwd(lib, opts=bd._opts(store_kind=1)) == bd.EUNSUPPORTED
     assert call_fwd(lib, opts=bd._opts(grid=-1)) == bd.EINVAL
     assert call_fwd(lib, opts=bd._opts(timeout_ns=-5)) == bd.EINVAL
 

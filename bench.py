@@ -188,7 +188,7 @@ def reference_arm(args):
     cfg = workloads.CONFIGS[args.config]
     cores = os.cpu_count() or 1
     torch.set_num_threads(cores)
-    rows_per_head, heads = 16, min(cfg.H, 8)
+    rows_per_head, heads = 64, min(cfg.H, 8)
     gen = torch.Generator().manual_seed(0)
 
     def draw(shape):
@@ -234,6 +234,10 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--config", default="video")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fused-only", action="store_true",
+                    help="time only the fused call (no attention-alone, serial or e2e legs); for profiling")
+    ap.add_argument("--H", type=int, default=None, help="override the head count (smaller profiling cases)")
+    ap.add_argument("--S", type=int, default=None, help="override the sequence length (smaller profiling cases)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -253,6 +257,10 @@ def main():
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     bd.load()
     cfg = workloads.CONFIGS[args.config]
+    overrides = {k: v for k, v in (("H", args.H), ("S", args.S)) if v is not None}
+    if overrides:
+        cfg = workloads.config(args.config, name=f"{args.config}_" + "_".join(f"{k}{v}" for k, v in overrides.items()),
+                               **overrides)
     stream = torch.cuda.current_stream()
 
     q, k, v = workloads.make_qkv(cfg, seed=rank, device="cuda")
@@ -304,6 +312,15 @@ def main():
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())} during the timed region")
 
+    if args.fused_only:
+        sampler.stop()
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "value": cfg.flops / (ms * 1e-3) / 1e12 * world,
+                              "unit": "TFLOP/s", "ms_per_step": ms, "steps": args.steps,
+                              "config": {"workload": cfg.name, "B": cfg.B, "H": cfg.H, "S": cfg.S,
+                                         "d": cfg.d, "P": cfg.P}, "clocks": clocks, "fused_only": True}),
+                  flush=True)
+        return 0
     # ---- attention alone and the serial baseline (same kernel, contiguous epilogue)
     ms_contig = time_events(contig, max(5, args.steps // 3), 2, stream)
     ms_permute = time_events(lambda: bd.attn_a2a_permute(o, cfg.P, parts, stream=stream),
@@ -351,9 +368,9 @@ def main():
     if not args.no_cpu_baseline:
         cores = os.cpu_count() or 1
         torch.set_num_threads(cores)
-        val, nrows, secs = cpu_oracle_sample(q, k, v, cfg, rows_per_head=32, heads=cfg.H, seed=0)
+        val, nrows, secs = cpu_oracle_sample(q, k, v, cfg, rows_per_head=256, heads=cfg.H, seed=0)
         cpu = {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-               "sample": f"{nrows} query rows (32 random rows x {cfg.H} heads) of this workload at full key "
+               "sample": f"{nrows} query rows (256 random rows x {cfg.H} heads) of this workload at full key "
                          f"length, float64 numpy oracle incl. the row's layout destination; "
                          f"{secs:.1f} s of CPU work; TFLOP/s = 4*S*d per row / time"}
     line = {

@@ -66,9 +66,9 @@ CONFIGS = {
 }
 
 
-def config(name: str, **overrides) -> AttnConfig:
+def config(preset: str, **overrides) -> AttnConfig:
     """A preset by name, optionally with fields replaced (e.g. a smaller S)."""
-    base = CONFIGS[name]
+    base = CONFIGS[preset]
     if not overrides:
         return base
     fields = dict(base.__dict__)

@@ -11,9 +11,24 @@ from oracle import attention as orc
 SENTINEL = -12345.0  # exactly representable in bf16
 GUARD = 256  # elements of guard band before and after each partition (16-byte multiple)
 
-# Tolerances of the fused path against the float64 oracle.
+# Tolerances of the fused path against the float64 oracle: max-abs 2e-2 on
+# top of the bf16 output format's own rounding (half a bf16 ulp of the exact
+# value; the exact result rounded to bf16 already differs from it by up to that
+# much, e.g. 0.029 at |O| = 8.16 in the joint preset), and relative
+# Frobenius 1e-2.
 MAX_ABS = 2e-2
 REL_FRO = 1e-2
+
+
+def half_ulp_bf16(x: np.ndarray) -> np.ndarray:
+    """Half a bf16 unit in the last place at |x| (8 significant bits)."""
+    ax = np.abs(x)
+    e = np.floor(np.log2(np.where(ax > 0, ax, 1.0)))
+    return np.where(ax > 0, np.exp2(e - 8), 0.0)
+
+
+def abs_tolerance(want: np.ndarray) -> np.ndarray:
+    return MAX_ABS + half_ulp_bf16(want)
 
 
 class GuardedPartitions:
@@ -44,7 +59,11 @@ def compare(got: np.ndarray, want: np.ndarray, what: str):
     mx = float(err.max()) if err.size else 0.0
     rf = rel_fro(got, want) if err.size else 0.0
     assert np.all(np.isfinite(got)), f"{what}: non-finite output"
-    assert mx <= MAX_ABS, f"{what}: max|err| {mx:.3e} > {MAX_ABS}"
+    if err.size:
+        excess = err - abs_tolerance(want)
+        i = np.unravel_index(int(np.argmax(excess)), err.shape)
+        assert excess[i] <= 0, (f"{what}: |err| {err[i]:.3e} at |ref| {abs(want[i]):.3f} exceeds "
+                                f"{MAX_ABS} + half bf16 ulp")
     assert rf <= REL_FRO, f"{what}: rel-Frobenius {rf:.3e} > {REL_FRO}"
     return mx, rf
 

@@ -1,0 +1,62 @@
+"""GPU tests of the Burst-Gap probe: the kernel's stamps are consistent
+(ordered, gaps honoured, both store kinds), a long gap brings the issue
+time down to its floor while no gap leaves a large burst drain-dominated,
+and the equation fitted on part of a small sweep predicts the rest."""
+import statistics
+
+import pytest
+import torch
+
+from attention_all_layout_gb300 import binding as bd
+from attention_all_layout_gb300 import burst_gap as bg
+from attention_all_layout_gb300 import probe_sweep as ps
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def prober():
+    K = bd.num_sms()
+    dst_bytes = (max(4 * ps.l2_bytes(), 256 * 2**20) // (4096 * K) + 1) * 4096 * K
+    return ps.Prober(dst_bytes, K * 64 * 3), K
+
+
+@pytest.mark.parametrize("kind", [0, 1])
+def test_stamps_are_ordered_and_gaps_honoured(prober, kind):
+    pr, K = prober
+    V = ps.round_volume(8 * 2**20, K)
+    G_ns = 5000
+    rounds = 16
+    st = pr.stamps[: K * rounds * 3]
+    st.zero_()
+    bd.xstage_probe_run(K, rounds, V, G_ns, pr.dst, st, store_kind=kind)
+    torch.cuda.synchronize()
+    s = st.view(K, rounds, 3).cpu()
+    assert torch.all(s[:, :, 1] >= s[:, :, 0])
+    assert torch.all(s[:, :, 2] - s[:, :, 1] >= G_ns)
+    assert torch.all(s[:, 1:, 0] >= s[:, :-1, 2])
+
+
+def test_fma_gap_kind_runs(prober):
+    pr, K = prober
+    p_short = pr.run(K, ps.round_volume(2**20, K), 0, 8, gap_kind=1, fma_iters=100)
+    p_long = pr.run(K, ps.round_volume(2**20, K), 0, 8, gap_kind=1, fma_iters=20000)
+    assert statistics.median(p_long.period) > statistics.median(p_short.period)
+
+
+def test_regimes_and_fit(prober):
+    pr, K = prober
+    pts = []
+    for vmb in (4, 32, 64):
+        V = ps.round_volume(vmb * 2**20, K)
+        for g in (0, 2, 5, 10, 20, 40):
+            pts.append(pr.run(K, V, g * 1000, 48))
+    big0 = next(p for p in pts if p.V == ps.round_volume(64 * 2**20, K) and p.G == 0)
+    big40 = next(p for p in pts if p.V == ps.round_volume(64 * 2**20, K) and p.G == 40e-6)
+    assert big0.t_iss_med > big40.t_iss_med
+    f = bg.fit(pts)
+    assert f.R > 0
+    res = bg.residuals(f, pts)
+    med = statistics.median(abs(r) for r in res)
+    print(f"probe fit: R = {f.R / 1e9:.0f} GB/s, Q = {f.Q}, median |rel| residual {med:.3f}")
+    assert med < 0.5

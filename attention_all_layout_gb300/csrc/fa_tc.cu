@@ -56,6 +56,12 @@ int launch_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv
              int grid, cudaStream_t stream) {
   auto kern = tc::fa_fwd_tc_kernel<D, A2A>;
   constexpr int smem = tc::Cfg<D>::SMEM_ALLOC;
+  // The in-kernel register split assumes exactly this launch register count;
+  // with fewer registers at launch the softmax warpgroups could never obtain
+  // their share, so refuse to launch rather than risk a stuck kernel.
+  cudaFuncAttributes attr;
+  if (cudaFuncGetAttributes(&attr, kern) != cudaSuccess) return ATTN_A2A_ECUDA;
+  if (attr.numRegs != tc::kLaunchRegs) return ATTN_A2A_EUNSUPPORTED;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return ATTN_A2A_ECUDA;
   kern<<<grid, tc::kThreads, smem, stream>>>(mq, mk, mv, p);

@@ -25,7 +25,8 @@
  *             start_j = sum of the earlier c_i (torch.tensor_split rule).
  *   math    : O[b,h] = softmax(scale * Q[b,h] K[b,h]^T) V[b,h]; fp32
  *             accumulation, probabilities rounded to bf16 before the P*V
- *             product, output rounded to bf16 (round to nearest even).
+ *             product and normalised by the sum of those rounded values,
+ *             output rounded to bf16 (round to nearest even).
  *
  * Conventions shared by every entry point:
  *   - Ownership: the caller owns every buffer. The library allocates no

@@ -16,8 +16,9 @@ import torch
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libattn_a2a.so")
 
-OK, EINVAL, EUNSUPPORTED, ECUDA, ETIMEOUT = 0, 1, 2, 3, 4
+OK, EINVAL, EUNSUPPORTED, ECUDA, ETIMEOUT, ETOOLARGE = 0, 1, 2, 3, 4, 5
 MAX_RANKS = 64
+NOALLOC_MAX_BYTES = 16 * 1024 * 1024  # XSTAGE_PROBE_NOALLOC_MAX_BYTES
 
 # Every symbol include/attn_a2a.h declares.
 EXPORTED = (
@@ -29,6 +30,7 @@ EXPORTED = (
     "attn_a2a_fwd_simt",
     "attn_a2a_fwd_host",
     "xstage_probe_run",
+    "xstage_probe_run_noalloc",
     "attn_a2a_strerror",
     "attn_a2a_num_sms",
 )
@@ -98,6 +100,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.attn_a2a_fwd_simt.argtypes = [vp, vp, vp, shp, cint, ctypes.c_float, pp, vp]
     lib.attn_a2a_fwd_host.argtypes = [vp, vp, vp, shp, cint, ctypes.c_float, vp, vp, vp, pp, pp, vp, vp]
     lib.xstage_probe_run.argtypes = [ctypes.POINTER(ProbeCfg), vp]
+    lib.xstage_probe_run_noalloc.argtypes = [ctypes.POINTER(ProbeCfg), vp]
     lib.attn_a2a_strerror.argtypes = [cint]
     lib.attn_a2a_strerror.restype = ctypes.c_char_p
     lib.attn_a2a_num_sms.argtypes = []
@@ -245,6 +248,18 @@ def xstage_probe_run(K: int, rounds: int, V_bytes: int, G_ns: int, dst: torch.Te
                    _ptr(dst), dst.numel() * dst.element_size(), _ptr(stamps), int(fma_iters))
     rc = lib.xstage_probe_run(ctypes.byref(cfg), _stream(stream))
     return _check(rc, "xstage_probe_run", check)
+
+
+def xstage_probe_run_noalloc(K: int, rounds: int, V_bytes: int, G_ns: int, stamps: torch.Tensor,
+                             store_kind: int = 0, gap_kind: int = 0, fma_iters: int = 0, stream=None,
+                             check: bool = True) -> int:
+    """The probe for callers that cannot allocate: the burst target is the library's fixed
+    16 MiB device array (no dst argument); per-round stamps land in `stamps`."""
+    lib = load()
+    cfg = ProbeCfg(int(K), int(rounds), int(V_bytes), int(G_ns), int(store_kind), int(gap_kind),
+                   None, 0, _ptr(stamps), int(fma_iters))
+    rc = lib.xstage_probe_run_noalloc(ctypes.byref(cfg), _stream(stream))
+    return _check(rc, "xstage_probe_run_noalloc", check)
 
 
 def attn_a2a_strerror(code: int) -> str:

@@ -155,6 +155,7 @@ const char* attn_a2a_strerror(int status) {
     case ATTN_A2A_EUNSUPPORTED: return "unsupported configuration";
     case ATTN_A2A_ECUDA: return "CUDA error";
     case ATTN_A2A_ETIMEOUT: return "bounded in-kernel wait expired";
+    case ATTN_A2A_ETOOLARGE: return "request exceeds the fixed scratch of the allocation-free entry point";
     default: return "unknown status";
   }
 }

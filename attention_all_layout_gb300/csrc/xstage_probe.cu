@@ -11,9 +11,15 @@
 // gap end. Stores are never waited for inside a round: the issuer only sees
 // the time it took to get them accepted, which is what the model predicts.
 #include <cstdint>
+#include <mutex>
 
 #include "internal.h"
 #include "ptx.cuh"
+
+// Burst target of xstage_probe_run_noalloc: fixed device memory inside the
+// library for callers that cannot allocate (include/attn_a2a.h explains who
+// and why). Every GPU that loads the library holds these 16 MiB until exit.
+static __device__ __align__(256) uint8_t g_noalloc_target[XSTAGE_PROBE_NOALLOC_MAX_BYTES];
 
 namespace attn_a2a {
 namespace {
@@ -92,4 +98,52 @@ int launch_probe(const xstage_probe_cfg& c, cudaStream_t stream) {
   return cudaGetLastError() == cudaSuccess ? ATTN_A2A_OK : ATTN_A2A_ECUDA;
 }
 
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::once_flag g_noalloc_once[kMaxDevices];
+void* g_noalloc_ptr[kMaxDevices];
+cudaError_t g_noalloc_err[kMaxDevices];
+
+// Device address of g_noalloc_target on the current device. In host code the
+// array's name is only a host-side stand-in, not an address a kernel may use;
+// the usable address comes from cudaGetSymbolAddress, looked up once per device
+// with that device current (the first call on each device does this set-up).
+int noalloc_target(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_A2A_ECUDA;
+  std::call_once(g_noalloc_once[dev], [dev] {
+    g_noalloc_err[dev] = cudaGetSymbolAddress(&g_noalloc_ptr[dev], g_noalloc_target);
+  });
+  if (g_noalloc_err[dev] != cudaSuccess || g_noalloc_ptr[dev] == nullptr) return ATTN_A2A_ECUDA;
+  *out = g_noalloc_ptr[dev];
+  return ATTN_A2A_OK;
+}
+
+}  // namespace
 }  // namespace attn_a2a
+
+// The probe without any device allocation: same kernel, burst target in the
+// library's fixed array instead of a caller buffer. No cudaMalloc, cudaFree or
+// allocating library call is made here.
+extern "C" int xstage_probe_run_noalloc(const xstage_probe_cfg* cfg, void* stream) {
+  using namespace attn_a2a;
+  if (cfg == nullptr) return ATTN_A2A_EINVAL;
+  const xstage_probe_cfg& c = *cfg;
+  if (c.K < 1 || c.K > 1024 || c.rounds < 1) return ATTN_A2A_EINVAL;
+  if (c.V_bytes <= 0 || c.V_bytes % (4096ll * c.K) != 0) return ATTN_A2A_EINVAL;
+  if (c.V_bytes > XSTAGE_PROBE_NOALLOC_MAX_BYTES) return ATTN_A2A_ETOOLARGE;
+  if (c.G_ns < 0 || c.store_kind < 0 || c.store_kind > 1 || c.gap_kind < 0 || c.gap_kind > 1)
+    return ATTN_A2A_EINVAL;
+  if (c.gap_kind == 1 && c.fma_iters < 0) return ATTN_A2A_EINVAL;
+  if (c.stamps == nullptr || (reinterpret_cast<uintptr_t>(c.stamps) & 7u) != 0) return ATTN_A2A_EINVAL;
+  void* target = nullptr;
+  const int rc = noalloc_target(&target);
+  if (rc != ATTN_A2A_OK) return rc;
+  // the bulk-copy source (32 KB) is within the default dynamic shared-memory limit
+  const int smem = c.store_kind == 1 ? kBulkChunk : 0;
+  xstage_probe_kernel<<<c.K, kProbeThreads, smem, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<uint8_t*>(target), XSTAGE_PROBE_NOALLOC_MAX_BYTES, c.V_bytes, c.rounds, c.G_ns,
+      c.store_kind, c.gap_kind, c.fma_iters, c.stamps);
+  return cudaGetLastError() == cudaSuccess ? ATTN_A2A_OK : ATTN_A2A_ECUDA;
+}

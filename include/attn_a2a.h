@@ -57,7 +57,9 @@ typedef enum {
   ATTN_A2A_EINVAL = 1,        /* bad argument (null, misaligned, out of range) */
   ATTN_A2A_EUNSUPPORTED = 2,  /* valid but not built (e.g. d not in {64,128}) */
   ATTN_A2A_ECUDA = 3,         /* CUDA runtime/driver error at launch */
-  ATTN_A2A_ETIMEOUT = 4       /* a bounded in-kernel wait expired (device status) */
+  ATTN_A2A_ETIMEOUT = 4,      /* a bounded in-kernel wait expired (device status) */
+  ATTN_A2A_ETOOLARGE = 5      /* request larger than the fixed scratch of an
+                                 allocation-free entry point */
 } attn_a2a_status;
 
 /* Problem shape and input strides (elements). d is contiguous. */
@@ -181,6 +183,38 @@ typedef struct {
 } xstage_probe_cfg;
 
 int xstage_probe_run(const xstage_probe_cfg* cfg, void* stream);
+
+/*
+ * xstage_probe_run_noalloc - the same probe for callers that cannot allocate
+ * device memory. (The pages have no counterpart: this is a deployment
+ * convenience.) Some callers may not call cudaMalloc at the point where they
+ * want to measure: a process whose device memory is owned entirely by another
+ * allocator (a framework's caching pool, a fixed arena reserved at start-up),
+ * or a runtime whose rules forbid allocation after initialisation. They still
+ * own the small stamps buffer, but not a burst target.
+ *
+ * Instead of cfg->dst, this entry point stores into a fixed device array that
+ * lives inside the library: XSTAGE_PROBE_NOALLOC_MAX_BYTES bytes (16 MiB),
+ * reserved on every GPU that loads the library until the process exits.
+ * cfg->dst and cfg->dst_bytes are ignored; every other field means what it
+ * means for xstage_probe_run. V_bytes above XSTAGE_PROBE_NOALLOC_MAX_BYTES
+ * returns ATTN_A2A_ETOOLARGE without launching. Because the target (16 MiB)
+ * is smaller than L2, this variant measures stores absorbed by L2, not the
+ * drain into HBM that a large caller-owned target measures.
+ *
+ * Set-up: the first call on each device looks up the device address of the
+ * array (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture. The call allocates nothing (no cudaMalloc,
+ * cudaFree or allocating library routine).
+ *
+ * Sharing: all calls on a device use the same array and it keeps the last
+ * call's contents. The probe only writes it, so nothing has to start at zero.
+ * Calls that overlap on the GPU (different streams, no ordering) race on the
+ * array, which makes their timings interfere; order them on one stream.
+ */
+#define XSTAGE_PROBE_NOALLOC_MAX_BYTES (16ll * 1024 * 1024)
+
+int xstage_probe_run_noalloc(const xstage_probe_cfg* cfg, void* stream);
 
 /* Static description of a status code. Never NULL. */
 const char* attn_a2a_strerror(int status);

@@ -134,3 +134,18 @@ def test_chunk_sizes_rule():
     assert bd.chunk_sizes(75600, 8) == [9450] * 8
     assert bd.chunk_sizes(10, 4) == [3, 3, 2, 2]
     assert bd.chunk_sizes(3, 8) == [1, 1, 1, 0, 0, 0, 0, 0]
+
+
+def test_noalloc_probe_validation(lib):
+    def run(**kw):
+        c = dict(K=4, rounds=3, V_bytes=4096 * 4, G_ns=0, store_kind=0, gap_kind=0, stamps=FAKE, fma_iters=0)
+        c.update(kw)
+        cfg = bd.ProbeCfg(c["K"], c["rounds"], c["V_bytes"], c["G_ns"], c["store_kind"], c["gap_kind"],
+                          None, 0, c["stamps"], c["fma_iters"])
+        return lib.xstage_probe_run_noalloc(ctypes.byref(cfg), None)
+
+    assert run(V_bytes=bd.NOALLOC_MAX_BYTES + 4096 * 4) == bd.ETOOLARGE
+    assert run(K=0) == bd.EINVAL
+    assert run(stamps=0) == bd.EINVAL
+    assert run(store_kind=3) == bd.EINVAL
+    assert "scratch" in bd.strerror(bd.ETOOLARGE)

@@ -6,7 +6,7 @@
 #include <cstdint>
 #include <cstring>
 
-#include "../../include/attn_a2a.h"
+#include "attn_a2a.h"
 #include "internal.h"
 
 namespace attn_a2a {

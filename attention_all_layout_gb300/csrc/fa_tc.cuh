@@ -48,6 +48,14 @@ constexpr int kBN = 128;  // keys per block
 constexpr int kThreads = 384;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: keep a stale row max until it lags by 2^8
+// Every kPolyEvery-th pair of probabilities is exponentiated on the FMA pipe
+// (exp2_poly_x2) instead of the MUFU; 0 = all on the MUFU. Off: GB300's MUFU
+// keeps up with the softmax here, and moving 1/8, 1/4 or 1/2 of the pairs to
+// the FMA pipe measured 2 %, 4 % and 9 % slower on the video shape.
+#ifndef ATTN_A2A_POLY_EVERY
+#define ATTN_A2A_POLY_EVERY 0
+#endif
+constexpr int kPolyEvery = ATTN_A2A_POLY_EVERY;
 // Register split (setmaxnreg): the kernel launches with kLaunchRegs per thread;
 // warpgroup 0 (producer, MMA issuer, two idle warps) gives registers back and
 // the two softmax warpgroups take them: 128*kRegsLow + 256*kRegsHigh must not
@@ -273,9 +281,14 @@ __device__ __forceinline__ float probs_half(const uint32_t (&sr)[128], uint32_t 
 #pragma unroll
   for (int i = 0; i < 32; ++i) {
     const int c = HALF * 64 + 2 * i;
-    float x0, x1;
+    float x0, x1, p0, p1;
     f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), scale2, bias2), x0, x1);
-    float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+    if (kPolyEvery > 0 && i % (kPolyEvery > 0 ? kPolyEvery : 1) == (kPolyEvery > 0 ? kPolyEvery - 1 : 0)) {
+      exp2_poly_x2(x0, x1, p0, p1);
+    } else {
+      p0 = ex2_approx(x0);
+      p1 = ex2_approx(x1);
+    }
     if (MASK) {
       p0 = c < valid ? p0 : 0.f;
       p1 = c + 1 < valid ? p1 : 0.f;

@@ -3,7 +3,7 @@
 
 #include <cuda_runtime.h>
 
-#include "../../include/attn_a2a.h"
+#include "attn_a2a.h"
 #include "epilogue.cuh"
 
 namespace attn_a2a {

@@ -1,0 +1,127 @@
+"""Issuer-visible overhead of the piggybacked all-to-all across sequence
+length, next to the Burst-Gap prediction and the two counterfactual models
+the X-Stage pages test against ("Results", FlashAttention-A2A optimisation:
+the fused kernel's overhead over attention alone stays flat and near zero as
+S grows, contradicting a completion-coupled model whose overhead grows with
+S; "Key Contributions": neither fully blocking nor unbounded-asynchronous
+models capture issuer-visible behaviour).
+
+For each S the same kernel runs with the all-to-all epilogue (fused) and with
+the contiguous epilogue (attention alone); the serial baseline adds the
+separate permute. The models, per work item of a CTA (two 128-row tiles, so
+V_item = 2 * 128 * 2d bytes of stores, and a compute gap G_item = the item's
+share of attention-alone time):
+
+  * Burst-Gap (pages' equation, fitted T0 and R from a probe sweep on this
+    GPU): the burst of all CTAs finishing an item together, V = n_SM * V_item,
+    costs the issuer T_iss = max(T0(V), V/R - G_item) per item;
+  * completion-coupled counterfactual: the issuer also waits until its stores
+    are drained, i.e. T0(V) + V/R per item;
+  * unbounded-asynchronous counterfactual: the issuer never waits: 0.
+Predicted overhead = items per SM * per-item cost, relative to attention
+alone. The measured overhead is t_fused / t_contig - 1.
+
+Usage: python -m attention_all_layout_gb300.overhead_report [--out FILE]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import sys
+
+import torch
+
+from . import binding as bd
+from . import burst_gap as bg
+from . import probe_sweep as ps
+from . import workloads
+
+S_LIST = (1024, 2048, 4096, 8192, 16384, 32768)
+
+
+def time_ms(fn, n):
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(n):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / n
+
+
+def fit_store_model():
+    """T0(V) table and R from a short probe sweep (st.global.v4, the epilogue's store kind)."""
+    K = bd.num_sms()
+    dst_bytes = (max(4 * ps.l2_bytes(), 256 * 2**20) // (4096 * K) + 1) * 4096 * K
+    pr = ps.Prober(dst_bytes, K * 64 * 3)
+    pts = []
+    for vmb in (1, 2, 4, 8, 16, 32, 64):
+        V = ps.round_volume(vmb * 2**20, K)
+        for g in (0, 1, 2, 4, 10, 40):
+            pts.append(pr.run(K, V, g * 1000, 48, store_kind=0))
+    f = bg.fit(pts)
+    table = sorted((V, t0) for (k, V, kind), t0 in f.T0.items())
+    return f.R, table
+
+
+def t0_of(table, V):
+    """Linear interpolation of the long-gap floor T0 at volume V."""
+    if V <= table[0][0]:
+        return table[0][1] * V / table[0][0]
+    for (v0, t0), (v1, t1) in zip(table, table[1:]):
+        if V <= v1:
+            return t0 + (t1 - t0) * (V - v0) / (v1 - v0)
+    return table[-1][1] * V / table[-1][0]
+
+
+def report(H=40, d=128, P=8):
+    R, table = fit_store_model()
+    n_sm = bd.num_sms()
+    rows = []
+    for S in S_LIST:
+        cfg = workloads.AttnConfig(f"S{S}", B=1, H=H, S=S, d=d, P=P)
+        q, k, v = workloads.make_qkv(cfg, seed=0, device="cuda")
+        parts = bd.alloc_partitions(1, S, H, d, P)
+        o = torch.empty((1, H, S, d), dtype=torch.bfloat16, device="cuda")
+        n = max(5, int(2e11 / cfg.flops * 50)) if cfg.flops < 2e11 else 10
+        t_f = time_ms(lambda: bd.attn_a2a_fwd(q, k, v, P, cfg.scale, parts), n)
+        t_c = time_ms(lambda: bd.attn_a2a_fwd_contig(q, k, v, cfg.scale, o), n)
+        t_p = time_ms(lambda: bd.attn_a2a_permute(o, P, parts), n)
+        items = H * ((S + 127) // 128 + 1) // 2
+        items_per_sm = -(-items // n_sm)
+        g_item = t_c * 1e-3 / items_per_sm
+        v_item = 2 * 128 * 2 * d
+        V = n_sm * v_item
+        t0 = t0_of(table, V)
+        burst_gap = bg.predict_t_iss(g_item, t0, V, R) * items_per_sm
+        coupled = (t0 + V / R) * items_per_sm
+        rows.append({"S": S, "fused_ms": t_f, "contig_ms": t_c, "permute_ms": t_p,
+                     "measured_overhead": t_f / t_c - 1, "serial_over_fused": (t_c + t_p) / t_f,
+                     "pred_burst_gap": burst_gap / (t_c * 1e-3),
+                     "pred_completion_coupled": coupled / (t_c * 1e-3),
+                     "pred_unbounded_async": 0.0, "items_per_sm": items_per_sm,
+                     "gap_item_us": g_item * 1e6, "burst_MB": V / 2**20})
+        del q, k, v, parts, o
+        torch.cuda.empty_cache()
+    return {"R_GBps": R / 1e9, "T0_table_us": [(V / 2**20, t * 1e6) for V, t in table], "H": H, "d": d,
+            "P": P, "rows": rows}
+
+
+def main(argv=None) -> int:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--out", default=None)
+    a = ap.parse_args(argv)
+    res = report()
+    text = json.dumps(res, indent=1)
+    if a.out:
+        with open(a.out, "w") as fh:
+            fh.write(text)
+    print(text)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

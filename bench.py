@@ -133,6 +133,23 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(mhz)}
 
 
+def max_over_ranks(ms: float, world: int, device) -> float:
+    """Slowest rank's time: the job finishes when its last replica does."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(flops_per_rank: float, world: int, max_ms: float) -> float:
+    """Whole-job TFLOP/s: the work of every replica over the slowest rank's time."""
+    return flops_per_rank * world / (max_ms * 1e-3) / 1e12
+
+
 def time_events(fn, steps, warmup, stream):
     import torch
 
@@ -301,13 +318,7 @@ def main():
     e1.record(stream)
     barrier()
     t_wall1 = time.time()
-    ms = e0.elapsed_time(e1) / args.steps
-    if world > 1:
-        import torch.distributed as dist
-
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, "cuda")
     clocks = sampler.summary(t_wall0, t_wall1)
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())} during the timed region")
@@ -354,7 +365,7 @@ def main():
     peaks, peak_src = load_peaks()
     flops = cfg.flops
     tflops = flops / (ms * 1e-3) / 1e12
-    total_value = tflops * world
+    total_value = job_throughput(flops, world, ms)
     peak = peaks["bf16_tflops"]
     traffic = recorded_traffic()
     if rank != 0:

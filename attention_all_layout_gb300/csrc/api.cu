@@ -184,6 +184,39 @@ int attn_a2a_fwd_contig(const void* q, const void* k, const void* v, const attn_
   return fwd_common(q, k, v, shp, 1, scale, nullptr, out, false, dev_status, nullptr, stream);
 }
 
+int attn_a2a_fwd_s2s(const void* const* q_parts, const void* const* k_parts,
+                     const void* const* v_parts, const attn_a2a_shape* shp, int P, float scale,
+                     void* const* out_partitions, int* dev_status, void* stream) {
+  if (shp == nullptr || q_parts == nullptr || k_parts == nullptr || v_parts == nullptr)
+    return ATTN_A2A_EINVAL;
+  if (shp->B < 0 || shp->H < 0 || shp->S < 0 || shp->d <= 0) return ATTN_A2A_EINVAL;
+  if (!std::isfinite(scale) || scale < 0.f) return ATTN_A2A_EINVAL;
+  if (shp->d != 64 && shp->d != 128) return ATTN_A2A_EUNSUPPORTED;
+  EpiParams epi;
+  int rc = make_partitions(*shp, P, out_partitions, &epi);
+  if (rc != ATTN_A2A_OK) return rc;
+  if (P > 8) return ATTN_A2A_EUNSUPPORTED;
+  if (static_cast<long long>(shp->B) * shp->H * shp->S == 0) return ATTN_A2A_OK;
+  if (static_cast<long long>(shp->B) * shp->H * ((shp->S + 255) / 256 + P) > (1ll << 30))
+    return ATTN_A2A_EUNSUPPORTED;
+  Span in[3 * 8];
+  int nin = 0;
+  for (int j = 0; j < P; ++j) {
+    const int c = epi.cbase + (j < epi.crem ? 1 : 0);
+    if (c == 0) continue;
+    const void* ptrs[3] = {q_parts[j], k_parts[j], v_parts[j]};
+    for (const void* ptr : ptrs) {
+      if (ptr == nullptr || !aligned16(ptr)) return ATTN_A2A_EINVAL;
+      const uintptr_t lo = reinterpret_cast<uintptr_t>(ptr);
+      in[nin++] = Span{lo, lo + static_cast<uintptr_t>(shp->B) * c * shp->H * shp->d * 2u};
+    }
+  }
+  if (partitions_alias_inputs(*shp, epi, in, nin)) return ATTN_A2A_EINVAL;
+  const attn_a2a_opts o = default_opts();
+  return launch_fa_tc_s2s(q_parts, k_parts, v_parts, *shp, scale, epi, dev_status, o,
+                          static_cast<cudaStream_t>(stream));
+}
+
 int attn_a2a_permute(const void* o, const attn_a2a_shape* shp, int P, void* const* out_partitions,
                      void* stream) {
   if (shp == nullptr || shp->B < 0 || shp->H < 0 || shp->S < 0) return ATTN_A2A_EINVAL;

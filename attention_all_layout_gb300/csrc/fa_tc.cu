@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <cmath>
+#include <cstring>
 #include <mutex>
 
 #include "fa_tc.cuh"
@@ -51,10 +52,9 @@ bool make_map(CUtensorMap* m, const void* base, int B, int H, int S, int d, long
   return r == CUDA_SUCCESS;
 }
 
-template <int D, bool A2A>
-int launch_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const tc::Params& p,
-             int grid, cudaStream_t stream) {
-  auto kern = tc::fa_fwd_tc_kernel<D, A2A>;
+template <int D, int MODE, int NMAP>
+int launch_t(const tc::Maps<NMAP>& maps, const tc::Params& p, int grid, cudaStream_t stream) {
+  auto kern = tc::fa_fwd_tc_kernel<D, MODE, NMAP>;
   constexpr int smem = tc::Cfg<D>::SMEM_ALLOC;
   // The in-kernel register split assumes exactly this launch register count;
   // with fewer registers at launch the softmax warpgroups could never obtain
@@ -64,8 +64,26 @@ int launch_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv
   if (attr.numRegs != tc::kLaunchRegs) return ATTN_A2A_EUNSUPPORTED;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return ATTN_A2A_ECUDA;
-  kern<<<grid, tc::kThreads, smem, stream>>>(mq, mk, mv, p);
+  kern<<<grid, tc::kThreads, smem, stream>>>(maps, p);
   return cudaGetLastError() == cudaSuccess ? ATTN_A2A_OK : ATTN_A2A_ECUDA;
+}
+
+void common_params(tc::Params& p, const attn_a2a_shape& shp, float scale, int* dev_status,
+                   const attn_a2a_opts& opts) {
+  p.B = shp.B;
+  p.H = shp.H;
+  p.S = shp.S;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.dev_status = dev_status;
+  p.timeout_ns = opts.timeout_ns > 0 ? static_cast<unsigned long long>(opts.timeout_ns) : 2000000000ull;
+  p.inject_stall = opts.inject_stall;
+  p.store_kind = opts.store_kind;
+}
+
+int grid_for(const tc::Params& p, const attn_a2a_opts& opts) {
+  int grid = opts.grid > 0 ? opts.grid : num_sms_current_device();
+  if (grid <= 0) return 0;
+  return grid > p.total ? p.total : grid;
 }
 
 }  // namespace
@@ -73,32 +91,54 @@ int launch_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv
 int launch_fa_tc(const void* q, const void* k, const void* v, const attn_a2a_shape& shp,
                  float scale, bool a2a, const EpiParams& epi, int* dev_status,
                  const attn_a2a_opts& opts, cudaStream_t stream) {
-  CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, q, shp.B, shp.H, shp.S, shp.d, shp.q_sb, shp.q_sh, shp.q_ss) ||
-      !make_map(&mk, k, shp.B, shp.H, shp.S, shp.d, shp.k_sb, shp.k_sh, shp.k_ss) ||
-      !make_map(&mv, v, shp.B, shp.H, shp.S, shp.d, shp.v_sb, shp.v_sh, shp.v_ss))
+  tc::Maps<1> maps;
+  if (!make_map(&maps.q[0], q, shp.B, shp.H, shp.S, shp.d, shp.q_sb, shp.q_sh, shp.q_ss) ||
+      !make_map(&maps.k[0], k, shp.B, shp.H, shp.S, shp.d, shp.k_sb, shp.k_sh, shp.k_ss) ||
+      !make_map(&maps.v[0], v, shp.B, shp.H, shp.S, shp.d, shp.v_sb, shp.v_sh, shp.v_ss))
     return ATTN_A2A_ECUDA;
   tc::Params p{};
-  p.B = shp.B;
-  p.H = shp.H;
-  p.S = shp.S;
+  common_params(p, shp, scale, dev_status, opts);
   p.nblk = (shp.S + tc::kBM - 1) / tc::kBM;
   p.npair = (p.nblk + 1) / 2;
   p.total = shp.B * shp.H * p.npair;
-  p.scale_log2 = scale * 1.4426950408889634f;
-  p.dev_status = dev_status;
-  p.timeout_ns = opts.timeout_ns > 0 ? static_cast<unsigned long long>(opts.timeout_ns) : 2000000000ull;
-  p.inject_stall = opts.inject_stall;
-  p.store_kind = opts.store_kind;
   p.epi = epi;
-  int grid = opts.grid > 0 ? opts.grid : num_sms_current_device();
+  const int grid = grid_for(p, opts);
   if (grid <= 0) return ATTN_A2A_ECUDA;
-  if (grid > p.total) grid = p.total;
   if (shp.d == 128)
-    return a2a ? launch_t<128, true>(mq, mk, mv, p, grid, stream)
-               : launch_t<128, false>(mq, mk, mv, p, grid, stream);
-  return a2a ? launch_t<64, true>(mq, mk, mv, p, grid, stream)
-             : launch_t<64, false>(mq, mk, mv, p, grid, stream);
+    return a2a ? launch_t<128, tc::kModeA2A, 1>(maps, p, grid, stream)
+               : launch_t<128, tc::kModeContig, 1>(maps, p, grid, stream);
+  return a2a ? launch_t<64, tc::kModeA2A, 1>(maps, p, grid, stream)
+             : launch_t<64, tc::kModeContig, 1>(maps, p, grid, stream);
+}
+
+int launch_fa_tc_s2s(const void* const* qp, const void* const* kp, const void* const* vp,
+                     const attn_a2a_shape& shp, float scale, const EpiParams& epi, int* dev_status,
+                     const attn_a2a_opts& opts, cudaStream_t stream) {
+  if (epi.P > tc::kMaxS2SRanks) return ATTN_A2A_EUNSUPPORTED;
+  tc::Maps<tc::kMaxS2SRanks> maps;
+  std::memset(&maps, 0, sizeof(maps));
+  const long long row = static_cast<long long>(shp.H) * shp.d;  // partition j is [B, c_j, H, d]
+  for (int j = 0; j < epi.P; ++j) {
+    const int c = epi.cbase + (j < epi.crem ? 1 : 0);
+    if (c == 0) continue;
+    const long long sb = row * c;
+    if (!make_map(&maps.q[j], qp[j], shp.B, shp.H, c, shp.d, sb, shp.d, row) ||
+        !make_map(&maps.k[j], kp[j], shp.B, shp.H, c, shp.d, sb, shp.d, row) ||
+        !make_map(&maps.v[j], vp[j], shp.B, shp.H, c, shp.d, sb, shp.d, row))
+      return ATTN_A2A_ECUDA;
+  }
+  tc::Params p{};
+  common_params(p, shp, scale, dev_status, opts);
+  p.nb_big = (epi.cbase + 1 + tc::kBM - 1) / tc::kBM;
+  p.nb_small = (epi.cbase + tc::kBM - 1) / tc::kBM;
+  p.nblk = epi.crem * p.nb_big + (epi.P - epi.crem) * p.nb_small;
+  p.npair = (p.nblk + 1) / 2;
+  p.total = shp.B * shp.H * p.npair;
+  p.epi = epi;
+  const int grid = grid_for(p, opts);
+  if (grid <= 0) return ATTN_A2A_ECUDA;
+  if (shp.d == 128) return launch_t<128, tc::kModeS2S, tc::kMaxS2SRanks>(maps, p, grid, stream);
+  return launch_t<64, tc::kModeS2S, tc::kMaxS2SRanks>(maps, p, grid, stream);
 }
 
 }  // namespace attn_a2a

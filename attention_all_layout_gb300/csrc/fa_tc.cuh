@@ -86,9 +86,26 @@ struct Cfg {
   static constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack for 1024-byte alignment
 };
 
+// Where the output tile goes and where the inputs come from:
+//   kModeContig  inputs [B,H,S,d] (strided), output [B,H,S,d] contiguous;
+//   kModeA2A     inputs [B,H,S,d] (strided), output P sequence-sharded
+//                partitions [B,c_j,H,d] (the post-attention all-to-all);
+//   kModeS2S     inputs AND output P sequence-sharded partitions: the
+//                pre-attention all-to-all is folded into the loads as well.
+//                Query tiles and key blocks are then counted per partition,
+//                starting at each partition's row 0, so that none straddles two
+//                partitions; only a partition's last block can be partial.
+enum : int { kModeContig = 0, kModeA2A = 1, kModeS2S = 2 };
+constexpr int kMaxS2SRanks = 8;
+
+template <int N>
+struct Maps {
+  CUtensorMap q[N], k[N], v[N];
+};
+
 struct Params {
   int B, H, S;
-  int nblk;   // ceil(S / 128): query blocks per head = key blocks
+  int nblk;   // query tiles per head = key blocks per head (ceil(S/128), or the per-partition count)
   int npair;  // ceil(nblk / 2): work items per head
   int total;  // B * H * npair
   float scale_log2;
@@ -96,8 +113,42 @@ struct Params {
   unsigned long long timeout_ns;
   int inject_stall;
   int store_kind;
+  int nb_big, nb_small;  // kModeS2S: 128-row blocks of a longer / shorter chunk
   EpiParams epi;
 };
+
+// 128-row block `idx` of a head: which tensor map holds it, its first row
+// there, and the row count of that map (so rows >= c do not exist).
+struct Blk {
+  int map, row, c;
+};
+
+template <int MODE>
+__device__ __forceinline__ Blk locate_block(const Params& p, int idx) {
+  Blk r;
+  if constexpr (MODE == kModeS2S) {
+    const int nbig = p.epi.crem * p.nb_big;
+    int j, blk;
+    if (idx < nbig) {
+      j = idx / p.nb_big;
+      blk = idx - j * p.nb_big;
+      r.c = p.epi.cbase + 1;
+    } else {
+      const int t = idx - nbig;
+      const int k = p.nb_small > 0 ? t / p.nb_small : 0;
+      j = p.epi.crem + k;
+      blk = t - k * p.nb_small;
+      r.c = p.epi.cbase;
+    }
+    r.map = j;
+    r.row = blk * kBM;
+  } else {
+    r.map = 0;
+    r.row = idx * kBM;
+    r.c = p.S;
+  }
+  return r;
+}
 
 struct Item {
   int b, h, pair;
@@ -113,9 +164,8 @@ __device__ __forceinline__ Item decode_item(const Params& p, int item) {
 }
 
 // ------------------------------------------------------------------ producer
-template <int D>
-__device__ void producer_role(const Params& p, const CUtensorMap* tmQ, const CUtensorMap* tmK,
-                              const CUtensorMap* tmV, uint32_t sbase, uint32_t bar0,
+template <int D, int MODE, int NMAP>
+__device__ void producer_role(const Params& p, const Maps<NMAP>* maps, uint32_t sbase, uint32_t bar0,
                               const WaitCtl& w) {
   using C = Cfg<D>;
   auto BAR = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
@@ -131,14 +181,18 @@ __device__ void producer_role(const Params& p, const CUtensorMap* tmQ, const CUt
       if (!mbar_wait(BAR(C::QE + t), (it & 1) ^ 1, w)) return false;
       mbar_arrive_expect_tx(BAR(C::QF + t), C::TILE_BYTES);
       const uint32_t dst = sbase + C::Q_OFF + t * C::TILE_BYTES;
-      const int row = (2 * wi.pair + t) * kBM;
+      int qt = 2 * wi.pair + t;  // past the last tile (odd count): rows past S read as zeros,
+      if (MODE == kModeS2S && qt >= p.nblk) qt = p.nblk - 1;  // or a real tile whose rows are not stored
+      const Blk bq = locate_block<MODE>(p, qt);
 #pragma unroll
       for (int a = 0; a < D / 64; ++a)
-        tma_load_4d(dst + a * C::ATOM_BYTES, tmQ, BAR(C::QF + t), a * 64, row, wi.h, wi.b, pol_q);
+        tma_load_4d(dst + a * C::ATOM_BYTES, &maps->q[bq.map], BAR(C::QF + t), a * 64, bq.row, wi.h, wi.b, pol_q);
       ++q_loads[t];
       return true;
     };
-    auto load_kv = [&](const CUtensorMap* m, int j) -> bool {
+    auto load_kv = [&](bool is_v, int j) -> bool {
+      const Blk bk = locate_block<MODE>(p, j);
+      const CUtensorMap* m = is_v ? &maps->v[bk.map] : &maps->k[bk.map];
       const uint32_t s = kv_it % C::NSTAGE;
       const uint32_t ph = (kv_it / C::NSTAGE) & 1;
       if (!mbar_wait(BAR(C::KVE + s), ph ^ 1, w)) return false;
@@ -146,12 +200,12 @@ __device__ void producer_role(const Params& p, const CUtensorMap* tmQ, const CUt
       const uint32_t dst = sbase + C::KV_OFF + s * C::TILE_BYTES;
 #pragma unroll
       for (int a = 0; a < D / 64; ++a)
-        tma_load_4d(dst + a * C::ATOM_BYTES, m, BAR(C::KVF + s), a * 64, j * kBN, wi.h, wi.b, pol_kv);
+        tma_load_4d(dst + a * C::ATOM_BYTES, m, BAR(C::KVF + s), a * 64, bk.row, wi.h, wi.b, pol_kv);
       ++kv_it;
       return true;
     };
-    ok = load_q(0) && load_kv(tmK, 0) && load_q(1) && load_kv(tmV, 0);
-    for (int j = 1; ok && j < p.nblk; ++j) ok = load_kv(tmK, j) && load_kv(tmV, j);
+    ok = load_q(0) && load_kv(false, 0) && load_q(1) && load_kv(true, 0);
+    for (int j = 1; ok && j < p.nblk; ++j) ok = load_kv(false, j) && load_kv(true, j);
   }
   if (!ok) {
     // Aborting: wait (bounded) for the copies this thread started, so none
@@ -303,7 +357,7 @@ __device__ __forceinline__ float probs_half(const uint32_t (&sr)[128], uint32_t 
   return s0 + s1;
 }
 
-template <int D, bool A2A>
+template <int D, int MODE>
 __device__ void softmax_role(const Params& p, int t, uint32_t bar0, uint32_t tmem, const WaitCtl& w) {
   using C = Cfg<D>;
   auto BAR = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
@@ -327,7 +381,8 @@ __device__ void softmax_role(const Params& p, int t, uint32_t bar0, uint32_t tme
       tc_fence_after();
       uint32_t sr[128];
       tmem_ld_x128(tS, sr);
-      const int valid = p.S - j * kBN;  // keys of this block that exist (>= 128 except at the end)
+      const Blk bk = locate_block<MODE>(p, j);
+      const int valid = bk.c - bk.row;  // keys of this block that exist (>= 128 except at the end)
       const float mx = valid >= kBN ? row_max<false>(sr, valid) : row_max<true>(sr, valid);
       const float m_new = mx * sl2;
       // Lazy rescaling: keep a stale row maximum until some row of the warp
@@ -386,9 +441,21 @@ __device__ void softmax_role(const Params& p, int t, uint32_t bar0, uint32_t tme
     else tmem_ld_x64(tO, o);
     tc_fence_before();
     mbar_arrive(BAR(C::OE + t));  // O_t may now be overwritten by the next item
-    if (srow < p.S) {
+    uint16_t* dst = nullptr;
+    if constexpr (MODE == kModeS2S) {
+      const int qt = 2 * wi.pair + t;
+      if (qt < p.nblk) {
+        const Blk bq = locate_block<MODE>(p, qt);
+        const int lrow = bq.row + r;
+        if (lrow < bq.c)
+          dst = static_cast<uint16_t*>(p.epi.part[bq.map]) +
+                ((static_cast<int64_t>(wi.b) * bq.c + lrow) * p.H + wi.h) * D;
+      }
+    } else if (srow < p.S) {
+      dst = out_row_ptr<D, MODE == kModeA2A>(p.epi, p.B, p.H, p.S, wi.b, wi.h, srow);
+    }
+    if (dst != nullptr) {
       const float inv_l = 1.0f / l;
-      uint16_t* dst = out_row_ptr<D, A2A>(p.epi, p.B, p.H, p.S, wi.b, wi.h, srow);
       uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
       for (int c = 0; c < D / 8; ++c) {
@@ -404,10 +471,9 @@ __device__ void softmax_role(const Params& p, int t, uint32_t bar0, uint32_t tme
 }
 
 // ------------------------------------------------------------------ kernel
-template <int D, bool A2A>
+template <int D, int MODE, int NMAP>
 __global__ void __launch_bounds__(kThreads, 1)
-    fa_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ Params p) {
+    fa_fwd_tc_kernel(const __grid_constant__ Maps<NMAP> maps, const __grid_constant__ Params p) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -438,9 +504,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tmQ);
-    tma_prefetch_desc(&tmK);
-    tma_prefetch_desc(&tmV);
+    const int nmaps = MODE == kModeS2S ? p.epi.P : 1;
+    for (int i = 0; i < nmaps; ++i) {
+      tma_prefetch_desc(&maps.q[i]);
+      tma_prefetch_desc(&maps.k[i]);
+      tma_prefetch_desc(&maps.v[i]);
+    }
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -455,13 +524,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
     if (warp == 0) {
-      if (lane == 0) producer_role<D>(p, &tmQ, &tmK, &tmV, sbase, bar0, w);
+      if (lane == 0) producer_role<D, MODE, NMAP>(p, &maps, sbase, bar0, w);
     } else if (warp == 1) {
       if (lane == 0) mma_role<D>(p, sbase, bar0, tmem, w);
     }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
-    softmax_role<D, A2A>(p, (warp - 4) / 4, bar0, tmem, w);
+    softmax_role<D, MODE>(p, (warp - 4) / 4, bar0, tmem, w);
   }
   tc_fence_before();
   __syncthreads();

@@ -20,6 +20,13 @@ int launch_fa_tc(const void* q, const void* k, const void* v, const attn_a2a_sha
                  float scale, bool a2a, const EpiParams& epi, int* dev_status,
                  const attn_a2a_opts& opts, cudaStream_t stream);
 
+// Sequence-sharded inputs (P partitions [B, c_j, H, d] each for q, k, v) and
+// sequence-sharded output partitions in epi; P <= 8.
+int launch_fa_tc_s2s(const void* const* q_parts, const void* const* k_parts,
+                     const void* const* v_parts, const attn_a2a_shape& shp, float scale,
+                     const EpiParams& epi, int* dev_status, const attn_a2a_opts& opts,
+                     cudaStream_t stream);
+
 int launch_fa_simt(const void* q, const void* k, const void* v, const attn_a2a_shape& shp,
                    float scale, const EpiParams& epi, cudaStream_t stream);
 

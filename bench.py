@@ -133,6 +133,15 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(mhz)}
 
 
+def _starts(S: int, P: int):
+    base, rem = divmod(S, P)
+    out, st = [], 0
+    for j in range(P):
+        out.append(st)
+        st += base + (1 if j < rem else 0)
+    return out
+
+
 def max_over_ranks(ms: float, world: int, device) -> float:
     """Slowest rank's time: the job finishes when its last replica does."""
     if world <= 1:
@@ -338,6 +347,16 @@ def main():
                              max(5, args.steps // 3), 2, stream)
     ms_serial = time_events(serial, max(5, args.steps // 3), 2, stream)
 
+    # ---- the whole Ulysses layer: sequence-sharded q, k, v in (pre-attention
+    # exchange folded into the loads), sequence-sharded output out
+    ms_s2s = None
+    if cfg.P <= 8:
+        sq, sk, sv = ([t[:, :, st:st + c].permute(0, 2, 1, 3).contiguous()
+                       for st, c in zip(_starts(cfg.S, cfg.P), bd.chunk_sizes(cfg.S, cfg.P))] for t in (q, k, v))
+        ms_s2s = time_events(lambda: bd.attn_a2a_fwd_s2s(sq, sk, sv, cfg.P, cfg.scale, parts, dev_status=status,
+                                                         stream=stream), max(5, args.steps // 3), 2, stream)
+        del sq, sk, sv
+
     # ---- e2e: host buffers through the C-ABI host entry point
     hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
     dq, dk, dv = (torch.empty_like(t) for t in (q, k, v))
@@ -411,6 +430,8 @@ def main():
         "serial_ms": ms_serial,
         "epilogue_overhead": ms / ms_contig - 1.0,
         "speedup_vs_serial": ms_serial / ms,
+        "ulysses_layer_s2s_ms": ms_s2s,
+        "ulysses_layer_s2s_tflops": (flops / (ms_s2s * 1e-3) / 1e12) if ms_s2s else None,
         "e2e": {"value": flops / (ms_e2e * 1e-3) / 1e12 * world, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": cfg.qkv_bytes, "d2h_bytes_per_step": cfg.out_bytes,
                 "ms_per_step": ms_e2e},

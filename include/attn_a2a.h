@@ -125,6 +125,30 @@ int attn_a2a_fwd_contig_ex(const void* q, const void* k, const void* v,
                            const attn_a2a_opts* opts, void* stream);
 
 /*
+ * attn_a2a_fwd_s2s - the whole Ulysses attention layer on virtual ranks:
+ * sequence-sharded q, k, v in, sequence-sharded output out. Ulysses
+ * sequence parallelism (the pages' FlashAttention-A2A setting) exchanges
+ * twice around attention: sequence -> head sharding before it, head ->
+ * sequence after it. attn_a2a_fwd folds the second exchange into the
+ * epilogue; this call also folds the first one into the loads: each CTA
+ * TMA-loads its Q, K and V tiles straight from the sequence-sharded input
+ * partitions, so neither exchange is a separate pass.
+ *   q_parts, k_parts, v_parts : HOST arrays of P device pointers; partition j
+ *                    of each is [B, c_j, H, d] bf16 contiguous (chunk rule as
+ *                    above; may be NULL if c_j == 0).
+ *   shp            : B, H, S (= sum of c_j), d; the strides are ignored.
+ *   P              : 1 <= P <= 8 (ATTN_A2A_EUNSUPPORTED beyond), H % P == 0.
+ *   out_partitions : as for attn_a2a_fwd.
+ * Query tiles and key blocks are taken per partition (each starts at a
+ * partition's first row), so when c_j is not a multiple of 128 the key
+ * blocks differ from attn_a2a_fwd's and the rounding may differ in the last
+ * bits; for c_j a multiple of 128 both calls are bit-identical.
+ */
+int attn_a2a_fwd_s2s(const void* const* q_parts, const void* const* k_parts,
+                     const void* const* v_parts, const attn_a2a_shape* shp, int P, float scale,
+                     void* const* out_partitions, int* dev_status, void* stream);
+
+/*
  * attn_a2a_permute - the serial all-to-all on its own: a pure copy of a
  * contiguous [B, H, S, d] bf16 device tensor o into the P partitions
  * (same layout and chunk rule as attn_a2a_fwd). shp supplies B, H, S, d; its

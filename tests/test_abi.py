@@ -149,3 +149,21 @@ def test_noalloc_probe_validation(lib):
     assert run(stamps=0) == bd.EINVAL
     assert run(store_kind=3) == bd.EINVAL
     assert "scratch" in bd.strerror(bd.ETOOLARGE)
+
+
+def test_s2s_validation(lib):
+    shp = bd.plain_shape(1, 16, 256, 64)
+    ptrs = lambda base, n: (ctypes.c_void_p * n)(*[FAKE * (base + j) for j in range(n)])
+    # P beyond the 8 tensor maps the kernel carries
+    assert lib.attn_a2a_fwd_s2s(ptrs(100, 16), ptrs(200, 16), ptrs(300, 16), ctypes.byref(shp), 16, 0.1,
+                                ptrs(400, 16), None, None) == bd.EUNSUPPORTED
+    # null input partition
+    q = ptrs(100, 2)
+    q[1] = None
+    assert lib.attn_a2a_fwd_s2s(q, ptrs(200, 2), ptrs(300, 2), ctypes.byref(shp), 2, 0.1, ptrs(400, 2),
+                                None, None) == bd.EINVAL
+    # output partition aliasing an input partition
+    assert lib.attn_a2a_fwd_s2s(ptrs(100, 2), ptrs(200, 2), ptrs(300, 2), ctypes.byref(shp), 2, 0.1,
+                                ptrs(200, 2), None, None) == bd.EINVAL
+    assert lib.attn_a2a_fwd_s2s(None, ptrs(200, 2), ptrs(300, 2), ctypes.byref(shp), 2, 0.1, ptrs(400, 2),
+                                None, None) == bd.EINVAL

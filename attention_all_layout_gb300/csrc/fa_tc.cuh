@@ -76,8 +76,7 @@ struct Cfg {
   static constexpr int KV_OFF = 2 * TILE_BYTES;
   static constexpr int BAR_OFF = KV_OFF + NSTAGE * TILE_BYTES;
   // barrier slots
-  // PF: probabilities of keys [0, 64) of the block published; PF2: keys [64, 128)
-  static constexpr int QF = 0, QE = 2, SF = 4, PF = 6, OF = 8, OE = 10, PF2 = 12, KVF = 14;
+  static constexpr int QF = 0, QE = 2, SF = 4, PF = 6, OF = 8, OE = 10, KVF = 12;
   static constexpr int KVE = KVF + NSTAGE;
   static constexpr int DONE = KVE + NSTAGE;
   static constexpr int NBAR = DONE + 1;
@@ -245,20 +244,17 @@ __device__ void mma_role(const Params& p, uint32_t sbase, uint32_t bar0, uint32_
   };
   // O_t (+)= P_t V_j. Returns false on abort.
   auto issue_pv = [&](int t, int j, uint32_t sV) -> bool {
-    const uint32_t vb = sbase + C::KV_OFF + sV * C::TILE_BYTES;
-    // keys [0, 64) as soon as their probabilities are in TMEM, then keys [64, 128)
-    if (j == 0 && !mbar_wait(BAR(C::OE + t), (it & 1) ^ 1, w)) return false;
-    for (int half = 0; half < 2; ++half) {
-      if (!mbar_wait(BAR((half == 0 ? C::PF : C::PF2) + t), pf_cnt[t] & 1, w)) return false;
-      tc_fence_after();
-#pragma unroll
-      for (int kk = half * 4; kk < half * 4 + 4; ++kk) {
-        umma_ts(tmem + 256 + t * D, tmem + t * 128 + kk * 8,
-                sdesc_sw128(vb + kk * 2048, C::ATOM_BYTES, 1024), kIdescPV,
-                (j > 0 || kk > 0) ? 1u : 0u);
-      }
-    }
+    if (!mbar_wait(BAR(C::PF + t), pf_cnt[t] & 1, w)) return false;
     ++pf_cnt[t];
+    if (j == 0 && !mbar_wait(BAR(C::OE + t), (it & 1) ^ 1, w)) return false;
+    tc_fence_after();
+    const uint32_t vb = sbase + C::KV_OFF + sV * C::TILE_BYTES;
+#pragma unroll
+    for (int kk = 0; kk < kBN / 16; ++kk) {
+      umma_ts(tmem + 256 + t * D, tmem + t * 128 + kk * 8,
+              sdesc_sw128(vb + kk * 2048, C::ATOM_BYTES, 1024), kIdescPV,
+              (j > 0 || kk > 0) ? 1u : 0u);
+    }
     if (t == 1) umma_commit(BAR(C::KVE + sV));  // V_j now read by both tiles
     if (j == p.nblk - 1) umma_commit(BAR(C::OF + t));
     return true;
@@ -321,22 +317,22 @@ __device__ __forceinline__ float row_max(const uint32_t (&sr)[128], int valid) {
   return max3f(a[0], a[1], fmaxf(a[2], a[3]));
 }
 
-// p_i = 2^(s_i * sl2 - m) for keys [64*HALF, 64*HALF + 64) of the block,
-// packed to bf16 pairs in pk[0..31]; returns the fp32 sum of the bf16 p_i.
-// Keys >= valid get p = 0 when MASK.
-template <bool MASK, int HALF>
-__device__ __forceinline__ float probs_half(const uint32_t (&sr)[128], uint32_t (&pk)[32], float sl2, float neg_m,
-                                            int valid) {
+// p_i = 2^(s_i * sl2 - m) for the 128 keys of the block, packed to bf16 pairs
+// in pk; returns the fp32 sum of the p_i (FlashAttention's convention: the
+// row sum is not rounded, the probabilities fed to P*V are). Keys >= valid
+// get p = 0 when MASK.
+template <bool MASK>
+__device__ __forceinline__ float probs(const uint32_t (&sr)[128], uint32_t (&pk)[64], float sl2, float neg_m,
+                                       int valid) {
   const uint64_t scale2 = f2_pack(sl2, sl2);
   const uint64_t bias2 = f2_pack(neg_m, neg_m);
   uint64_t acc[4];
 #pragma unroll
   for (int a = 0; a < 4; ++a) acc[a] = f2_pack(0.f, 0.f);
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    const int c = HALF * 64 + 2 * i;
+  for (int i = 0; i < 64; ++i) {
     float x0, x1, p0, p1;
-    f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), scale2, bias2), x0, x1);
+    f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1])), scale2, bias2), x0, x1);
     if (kPolyEvery > 0 && i % (kPolyEvery > 0 ? kPolyEvery : 1) == (kPolyEvery > 0 ? kPolyEvery - 1 : 0)) {
       exp2_poly_x2(x0, x1, p0, p1);
     } else {
@@ -344,13 +340,11 @@ __device__ __forceinline__ float probs_half(const uint32_t (&sr)[128], uint32_t 
       p1 = ex2_approx(x1);
     }
     if (MASK) {
-      p0 = c < valid ? p0 : 0.f;
-      p1 = c + 1 < valid ? p1 : 0.f;
+      p0 = 2 * i < valid ? p0 : 0.f;
+      p1 = 2 * i + 1 < valid ? p1 : 0.f;
     }
+    acc[i & 3] = f2_add(acc[i & 3], f2_pack(p0, p1));
     pk[i] = pack_bf16x2(p0, p1);
-    // sum the bf16-rounded values, i.e. exactly what the P*V product uses, so
-    // that the normalised output is a convex combination of rows of V
-    acc[i & 3] = f2_add(acc[i & 3], f2_pack(__uint_as_float(pk[i] << 16), __uint_as_float(pk[i] & 0xffff0000u)));
   }
   float s0, s1;
   f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), s0, s1);
@@ -412,25 +406,11 @@ __device__ void softmax_role(const Params& p, int t, uint32_t bar0, uint32_t tme
         l *= alpha;
         m_used = m_tgt;
       }
-      // Publish P in two halves so that the MMA on keys [0, 64) overlaps the
-      // exponentials of keys [64, 128).
-      const bool stall = p.inject_stall && t == 0 && j == 0 && it == 0;  // test hook
-      {
-        uint32_t pk[32];
-        l += valid >= kBN ? probs_half<false, 0>(sr, pk, sl2, -m_used, valid)
-                          : probs_half<true, 0>(sr, pk, sl2, -m_used, valid);
-        tmem_st_x32(tS, pk);
-        tc_fence_before();
-        if (!stall) mbar_arrive(BAR(C::PF + t));
-      }
-      {
-        uint32_t pk[32];
-        l += valid >= kBN ? probs_half<false, 1>(sr, pk, sl2, -m_used, valid)
-                          : probs_half<true, 1>(sr, pk, sl2, -m_used, valid);
-        tmem_st_x32(tS + 32, pk);
-        tc_fence_before();
-        if (!stall) mbar_arrive(BAR(C::PF2 + t));
-      }
+      uint32_t pk[64];
+      l += valid >= kBN ? probs<false>(sr, pk, sl2, -m_used, valid) : probs<true>(sr, pk, sl2, -m_used, valid);
+      tmem_st_x64(tS, pk);
+      tc_fence_before();
+      if (!(p.inject_stall && t == 0 && j == 0 && it == 0)) mbar_arrive(BAR(C::PF + t));  // test hook
     }
     // ---- epilogue: the tile owner stores its rows to their destination and moves on
     const bool got = __all_sync(0xffffffffu, mbar_wait(BAR(C::OF + t), it & 1, w));
@@ -491,7 +471,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(BAR(C::QE + t), 1);
       mbar_init(BAR(C::SF + t), 1);
       mbar_init(BAR(C::PF + t), kBM);
-      mbar_init(BAR(C::PF2 + t), kBM);
       mbar_init(BAR(C::OF + t), 1);
       mbar_init(BAR(C::OE + t), kBM);
     }

@@ -24,9 +24,9 @@
  *             ("sequence-sharded"). c_j = floor(S/P) + (j < S mod P ? 1 : 0),
  *             start_j = sum of the earlier c_i (torch.tensor_split rule).
  *   math    : O[b,h] = softmax(scale * Q[b,h] K[b,h]^T) V[b,h]; fp32
- *             accumulation, probabilities rounded to bf16 before the P*V
- *             product and normalised by the sum of those rounded values,
- *             output rounded to bf16 (round to nearest even).
+ *             accumulation and row sums, probabilities rounded to bf16
+ *             before the P*V product, output rounded to bf16 (round to
+ *             nearest even).
  *
  * Conventions shared by every entry point:
  *   - Ownership: the caller owns every buffer. The library allocates no

@@ -126,7 +126,11 @@ def test_scale_zero_and_constant_v():
     compare(got, np.broadcast_to(mean, got.shape), "scale 0")
     vc = torch.full_like(v, 0.75)
     g = fused(q, k, vc, P, 1.0)
-    assert torch.all(torch.cat([p.flatten() for p in g.parts]) == 0.75)
+    got = partitions_to_bhsd(g.parts)
+    compare(got, np.full(got.shape, 0.75), "constant V")
+    # the rows sum bf16-rounded probabilities against an fp32 row sum, so a
+    # constant comes back within P's rounding (2^-8 relative), not exactly
+    assert np.abs(got - 0.75).max() <= 0.75 * 2.0 ** -8 + 2.0 ** -10
 
 
 def test_empty_sequence_launches_nothing():

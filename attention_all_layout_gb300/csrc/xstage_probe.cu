@@ -10,6 +10,9 @@
 // last store of the burst has been issued by every thread of the CTA, and at
 // gap end. Stores are never waited for inside a round: the issuer only sees
 // the time it took to get them accepted, which is what the model predicts.
+// The gap is either idle time, a dependent FMA chain, or tensor-core work
+// (tcgen05.mma into TMEM, issued once the burst is out): with the latter the
+// issue time of each round is exactly how long the MMA pipe stalls.
 #include <cstdint>
 #include <mutex>
 
@@ -26,6 +29,11 @@ namespace {
 
 constexpr int kProbeThreads = 512;
 constexpr int kBulkChunk = 32768;  // bytes of the shared-memory source of each bulk copy
+// gap_kind 2: operands (two 128 x 64 bf16 swizzle atoms) at a 1024-byte aligned
+// offset after the bulk source, then an mbarrier and the TMEM address slot.
+constexpr int kMmaOperandBytes = 2 * 16384;
+constexpr int kMmaSmem = kBulkChunk + 1024 + kMmaOperandBytes + 64;
+constexpr uint32_t kMmaTmemCols = 128;
 
 __global__ void __launch_bounds__(kProbeThreads)
     xstage_probe_kernel(uint8_t* __restrict__ dst, long long dst_bytes, long long V, int rounds,
@@ -42,6 +50,31 @@ __global__ void __launch_bounds__(kProbeThreads)
   }
   float acc = 1.0f + 1e-3f * threadIdx.x;
   uint64_t t0 = 0, t1 = 0, t2 = 0;
+  // gap_kind 2 set-up: zeroed operands, one mbarrier, 128 TMEM columns
+  uint32_t ops = 0, mbar = 0, tmem = 0;
+  uint32_t* tslot = nullptr;
+  if (gap_kind == 2) {
+    const uint32_t raw = smem_u32(bulk_src) + kBulkChunk;
+    ops = (raw + 1023u) & ~1023u;
+    uint8_t* gops = bulk_src + (ops - smem_u32(bulk_src));
+    for (int i = threadIdx.x; i < kMmaOperandBytes / 4; i += blockDim.x) reinterpret_cast<uint32_t*>(gops)[i] = 0u;
+    mbar = ops + kMmaOperandBytes;
+    tslot = reinterpret_cast<uint32_t*>(gops + kMmaOperandBytes + 8);
+    if (threadIdx.x == 0) {
+      mbar_init(mbar, 1);
+      fence_mbar_init();
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    if (threadIdx.x < 32) {
+      tmem_alloc(smem_u32(tslot), kMmaTmemCols);
+      tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    tmem = *tslot;
+  }
+  uint32_t mma_phase = 0;
   for (int r = 0; r < rounds; ++r) {
     __syncthreads();
     if (threadIdx.x == 0) t0 = globaltimer_ns();
@@ -68,8 +101,21 @@ __global__ void __launch_bounds__(kProbeThreads)
       if (threadIdx.x == 0)
         while (globaltimer_ns() - t1 < static_cast<uint64_t>(G_ns)) {
         }
-    } else {
+    } else if (gap_kind == 1) {
       for (long long i = 0; i < fma_iters; ++i) acc = fmaf(acc, 0.99999988f, 1.1920929e-7f);
+    } else if (threadIdx.x == 0) {
+      // fma_iters tcgen05.mma of 128 x 128 x 16 (bf16 in, fp32 in TMEM), then
+      // wait (bounded, 1 s) for them to finish
+      constexpr uint32_t idesc = idesc_bf16_f32(128, 128, false, false);
+      tc_fence_after();
+      for (long long i = 0; i < fma_iters; ++i) {
+        const uint32_t off = static_cast<uint32_t>(i & 3) * 32;
+        umma_ss(tmem, sdesc_sw128(ops + off, 16, 1024), sdesc_sw128(ops + 16384 + off, 16, 1024), idesc,
+                i > 0 ? 1u : 0u);
+      }
+      umma_commit(mbar);
+      mbar_wait_drain(mbar, mma_phase, 1000000000ull);
+      mma_phase ^= 1u;
     }
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -82,12 +128,20 @@ __global__ void __launch_bounds__(kProbeThreads)
   }
   if (store_kind == 1 && threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
   if (acc == 1234.5f) dst[0] = 1;  // keeps the gap's FMA chain from being removed
+  if (gap_kind == 2) {
+    tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x < 32) {
+      tc_fence_after();
+      tmem_dealloc(tmem, kMmaTmemCols);
+    }
+  }
 }
 
 }  // namespace
 
 int launch_probe(const xstage_probe_cfg& c, cudaStream_t stream) {
-  const int smem = c.store_kind == 1 ? kBulkChunk : 0;
+  const int smem = c.gap_kind == 2 ? kMmaSmem : (c.store_kind == 1 ? kBulkChunk : 0);
   if (smem > 0 &&
       cudaFuncSetAttribute(xstage_probe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
           cudaSuccess)

@@ -47,6 +47,44 @@ class Prober:
                         first=first)
 
 
+def measured_gap(p: bg.Point) -> float:
+    """Median gap actually spent per round (period - issue time), seconds."""
+    return statistics.median([per - iss for per, iss in zip(p.period, p.t_iss)])
+
+
+def sweep_mma_gap(pr: "Prober", K: int, vmbs=(8, 32, 64), gaps_us=(0, 1, 2, 4, 6, 8, 12, 20),
+                  kinds=(0, 1), rounds: int = 48):
+    """Burst-Gap check with tensor-core work as the gap (gap_kind 2): each
+    round issues its stores, then tcgen05 MMAs that the producer waits for, so
+    the issue time is the MMA pipe's stall. G is the measured gap."""
+    V0 = ps_round(K)
+    cal = pr.run(K, V0, 0, 16, gap_kind=2, fma_iters=4000)
+    ns_per_mma = max(measured_gap(cal) * 1e9, 1.0) / 4000
+    pts = []
+    for kind in kinds:
+        for vmb in vmbs:
+            V = round_volume(vmb * 2**20, K)
+            for g in gaps_us:
+                n = int(round(g * 1000 / ns_per_mma))
+                p = pr.run(K, V, 0, rounds, store_kind=kind, gap_kind=2, fma_iters=n)
+                p.G = measured_gap(p)
+                pts.append(p)
+    f = bg.fit(pts)
+    res = bg.residuals(f, pts)
+    return {
+        "ns_per_mma_128x128x16": ns_per_mma,
+        "fit": {"R_GBps": f.R / 1e9, "Q_MB": None if f.Q is None else f.Q / 2**20},
+        "median_abs_rel": statistics.median(abs(r) for r in res),
+        "max_abs_rel": max(abs(r) for r in res),
+        "points": [{"V_MB": p.V / 2**20, "kind": p.store_kind, "G_us": p.G * 1e6, "stall_us": p.t_iss_med * 1e6,
+                    "pred_us": f.predict(p) * 1e6} for p in pts],
+    }
+
+
+def ps_round(K: int) -> int:
+    return 4096 * K
+
+
 def l2_bytes() -> int:
     return int(torch.cuda.get_device_properties(0).L2_cache_size)
 
@@ -71,6 +109,8 @@ def sweep(quick: bool = False, kinds=(0, 1), rounds: int = 64, seed: int = 0) ->
         V = round_volume(8 * 2**20, k)
         p = pr.run(k, V, 20000, rounds, store_kind=0)
         t0_k.append({"K": k, "V": V, "t0_us": p.t_iss_med * 1e6})
+    mma = sweep_mma_gap(pr, K, rounds=max(16, rounds // 2)) if not quick else sweep_mma_gap(
+        pr, K, vmbs=(16, 64), gaps_us=(0, 2, 6, 20), rounds=32)
     # calibration / held-out split: every third G value is held out
     rnd = random.Random(seed)
     held, cal = [], []
@@ -89,6 +129,7 @@ def sweep(quick: bool = False, kinds=(0, 1), rounds: int = 64, seed: int = 0) ->
                     "max_abs_rel": max((abs(r) for r in res), default=None),
                     "frac_within_15pct": (sum(abs(r) <= 0.15 for r in res) / len(res)) if res else None},
         "t0_vs_K": t0_k,
+        "mma_gap": mma,
         "points": [{"V_MB": p.V / 2**20, "G_us": p.G * 1e6, "kind": p.store_kind, "t_iss_us": p.t_iss_med * 1e6,
                     "period_us": p.period_med * 1e6, "first_us": p.first * 1e6,
                     "pred_us": f.predict(p) * 1e6 if (p.K, p.V, p.store_kind) in f.T0 else None}
@@ -108,6 +149,7 @@ def main(argv=None) -> int:
         with open(a.out, "w") as fh:
             fh.write(text)
     print(json.dumps({k: res[k] for k in ("K", "fit", "heldout", "t0_vs_K")}, indent=1))
+    print(json.dumps({k: v for k, v in res["mma_gap"].items() if k != "points"}, indent=1))
     return 0
 
 

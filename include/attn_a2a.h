@@ -199,11 +199,16 @@ typedef struct {
                             1: cp.async.bulk from shared memory, issued by one thread */
   int gap_kind;          /* 0: spin on %globaltimer for G_ns (the issuer stays idle);
                             1: dependent FMA chain on every producer thread sized by the
-                               host to last about G_ns (the issuer computes) */
+                               host to last about G_ns (the issuer computes);
+                            2: tensor-core work: fma_iters tcgen05.mma of 128x128x16
+                               (bf16, fp32 accumulate in TMEM) issued after the burst and
+                               waited for, so each round's issue time is the MMA pipe's
+                               stall (G_ns is ignored for kinds 1 and 2) */
   void* dst;             /* device scratch target, 16-byte aligned */
   long long dst_bytes;   /* >= V_bytes, multiple of 4096*K */
   long long* stamps;     /* device int64 [K][rounds][3] */
-  long long fma_iters;   /* gap_kind 1: dependent FMAs per thread per gap (host-calibrated) */
+  long long fma_iters;   /* gap_kind 1: dependent FMAs per thread per gap; gap_kind 2: MMA
+                            instructions per gap (both host-calibrated, <= 1e8) */
 } xstage_probe_cfg;
 
 int xstage_probe_run(const xstage_probe_cfg* cfg, void* stream);

@@ -60,3 +60,21 @@ def test_regimes_and_fit(prober):
     med = statistics.median(abs(r) for r in res)
     print(f"probe fit: R = {f.R / 1e9:.0f} GB/s, Q = {f.Q}, median |rel| residual {med:.3f}")
     assert med < 0.5
+
+
+@pytest.mark.parametrize("kind", [0, 1])
+def test_mma_gap_kind(prober, kind):
+    """Tensor-core work as the gap: stamps stay ordered, more MMAs make a longer
+    gap, and a drain-dominated burst stalls the MMA pipe longer with no work
+    behind it than with a long MMA gap."""
+    pr, K = prober
+    V = ps.round_volume(64 * 2**20, K)
+    short = pr.run(K, V, 0, 24, store_kind=kind, gap_kind=2, fma_iters=0)
+    long = pr.run(K, V, 0, 24, store_kind=kind, gap_kind=2, fma_iters=2000)
+    assert ps.measured_gap(long) > ps.measured_gap(short)
+    assert short.t_iss_med >= long.t_iss_med
+    st = pr.stamps[: K * 8 * 3]
+    bd.xstage_probe_run(K, 8, V, 0, pr.dst, st, store_kind=kind, gap_kind=2, fma_iters=500)
+    torch.cuda.synchronize()
+    s = st.view(K, 8, 3).cpu()
+    assert torch.all(s[:, :, 1] >= s[:, :, 0]) and torch.all(s[:, :, 2] >= s[:, :, 1])

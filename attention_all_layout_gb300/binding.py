@@ -50,7 +50,8 @@ class Opts(ctypes.Structure):
         ("grid", ctypes.c_int),
         ("timeout_ns", ctypes.c_longlong),
         ("inject_stall", ctypes.c_int),
-        ("reserved", ctypes.c_int * 3),
+        ("tile_order", ctypes.c_int),
+        ("reserved", ctypes.c_int * 2),
     ]
 
 
@@ -176,8 +177,8 @@ def _ptr_array(tensors: Sequence[Optional[torch.Tensor]]):
     return arr
 
 
-def _opts(store_kind=0, grid=0, timeout_ns=0, inject_stall=0) -> Opts:
-    return Opts(store_kind, grid, timeout_ns, inject_stall, (ctypes.c_int * 3)(0, 0, 0))
+def _opts(store_kind=0, grid=0, timeout_ns=0, inject_stall=0, tile_order=0) -> Opts:
+    return Opts(store_kind, grid, timeout_ns, inject_stall, tile_order, (ctypes.c_int * 2)(0, 0))
 
 
 def _check(code: int, what: str, check: bool) -> int:
@@ -189,12 +190,12 @@ def _check(code: int, what: str, check: bool) -> int:
 # ------------------------------------------------------------------ entry points (same names as the C ABI)
 def attn_a2a_fwd(q, k, v, P: int, scale: float, out_partitions, dev_status=None, stream=None,
                  store_kind: int = 0, grid: int = 0, timeout_ns: int = 0, inject_stall: int = 0,
-                 check: bool = True) -> int:
+                 tile_order: int = 0, check: bool = True) -> int:
     """Fused attention + head->sequence all-to-all into `out_partitions` (P tensors [B,c_j,H,d])."""
     lib = load()
     shp = shape_of(q, k, v)
     parts = _ptr_array(out_partitions)
-    opts = _opts(store_kind, grid, timeout_ns, inject_stall)
+    opts = _opts(store_kind, grid, timeout_ns, inject_stall, tile_order)
     rc = lib.attn_a2a_fwd_ex(_ptr(q), _ptr(k), _ptr(v), ctypes.byref(shp), int(P), float(scale), parts,
                              _ptr(dev_status), ctypes.byref(opts), _stream(stream))
     return _check(rc, "attn_a2a_fwd", check)

@@ -110,7 +110,8 @@ int fwd_common(const void* q, const void* k, const void* v, const attn_a2a_shape
   int rc = check_inputs(q, k, v, shp, scale, &empty);
   if (rc != ATTN_A2A_OK) return rc;
   if (opts != nullptr && (opts->store_kind < 0 || opts->store_kind > 1 || opts->grid < 0 ||
-                          opts->timeout_ns < 0 || opts->inject_stall < 0 || opts->inject_stall > 1))
+                          opts->timeout_ns < 0 || opts->inject_stall < 0 || opts->inject_stall > 1 ||
+                          opts->tile_order < 0 || opts->tile_order > 1))
     return ATTN_A2A_EINVAL;
   if (opts != nullptr && opts->store_kind != 0) return ATTN_A2A_EUNSUPPORTED;  // bulk epilogue not built
   EpiParams epi;

@@ -102,6 +102,9 @@ int launch_fa_tc(const void* q, const void* k, const void* v, const attn_a2a_sha
   p.npair = (p.nblk + 1) / 2;
   p.total = shp.B * shp.H * p.npair;
   p.epi = epi;
+  // chunk-interleaved order: only when every chunk holds the same whole number of pairs
+  if (opts.tile_order == 1 && a2a && epi.P > 1 && epi.crem == 0 && epi.cbase % (2 * tc::kBM) == 0)
+    p.interleave = epi.cbase / (2 * tc::kBM);
   const int grid = grid_for(p, opts);
   if (grid <= 0) return ATTN_A2A_ECUDA;
   if (shp.d == 128)

@@ -113,6 +113,7 @@ struct Params {
   int inject_stall;
   int store_kind;
   int nb_big, nb_small;  // kModeS2S: 128-row blocks of a longer / shorter chunk
+  int interleave;        // > 1: chunk-interleaved item order with this many pairs per chunk
   EpiParams epi;
 };
 
@@ -156,6 +157,12 @@ struct Item {
 __device__ __forceinline__ Item decode_item(const Params& p, int item) {
   Item it;
   it.pair = item % p.npair;
+  if (p.interleave > 1) {
+    // i-th item of a head -> pair (i mod P) * pairs_per_chunk + i / P: neighbouring
+    // items (run at the same time by neighbouring CTAs) land in different chunks
+    const int P = p.npair / p.interleave;
+    it.pair = (it.pair % P) * p.interleave + it.pair / P;
+  }
   const int bh = item / p.npair;
   it.h = bh % p.H;
   it.b = bh / p.H;

@@ -110,11 +110,38 @@ def report(H=40, d=128, P=8):
             "P": P, "rows": rows}
 
 
+def order_comparison(names=("image", "joint", "video")):
+    """Sequence-order vs chunk-interleaved work items (burst shaping): same
+    results, different store pattern. With the epilogue's bursts far past the
+    Burst-Gap knee the model predicts no difference."""
+    out = []
+    for name in names:
+        cfg = workloads.CONFIGS[name]
+        q, k, v = workloads.make_qkv(cfg, seed=0, device="cuda")
+        parts = bd.alloc_partitions(cfg.B, cfg.S, cfg.H, cfg.d, cfg.P)
+        n = 10 if cfg.flops > 1e13 else 100
+        t = [time_ms(lambda o=o: bd.attn_a2a_fwd(q, k, v, cfg.P, cfg.scale, parts, tile_order=o), n) for o in (0, 1)]
+        out.append({"config": name, "sequence_order_ms": t[0], "chunk_interleaved_ms": t[1],
+                    "interleaved_over_sequence": t[1] / t[0]})
+        del q, k, v, parts
+        torch.cuda.empty_cache()
+    return out
+
+
 def main(argv=None) -> int:
     ap = argparse.ArgumentParser()
     ap.add_argument("--out", default=None)
+    ap.add_argument("--orders-only", action="store_true", help="only the burst-shaping order comparison")
     a = ap.parse_args(argv)
+    if a.orders_only:
+        res = {"orders": order_comparison()}
+        print(json.dumps(res, indent=1))
+        if a.out:
+            with open(a.out, "w") as fh:
+                fh.write(json.dumps(res, indent=1))
+        return 0
     res = report()
+    res["orders"] = order_comparison()
     text = json.dumps(res, indent=1)
     if a.out:
         with open(a.out, "w") as fh:

@@ -82,7 +82,13 @@ typedef struct {
                            query tile withholds its first "probabilities ready" signal,
                            so the MMA role's bounded wait expires and the kernel reports
                            ATTN_A2A_ETIMEOUT through dev_status and exits cleanly */
-  int reserved[3];
+  int tile_order;       /* order of a head's work items (pairs of 128-row query tiles):
+                           0 = sequence order (consecutive items write to the same
+                           destination partition); 1 = chunk-interleaved: consecutive
+                           items cycle through the P destination partitions, spreading
+                           each wave's store burst over all of them (burst shaping).
+                           Results are identical; only the store pattern changes */
+  int reserved[2];
 } attn_a2a_opts;
 
 /*

@@ -91,6 +91,7 @@ def test_bad_options_rejected(lib):
     assert call_fwd(lib, opts=bd._opts(store_kind=1)) == bd.EUNSUPPORTED
     assert call_fwd(lib, opts=bd._opts(grid=-1)) == bd.EINVAL
     assert call_fwd(lib, opts=bd._opts(timeout_ns=-5)) == bd.EINVAL
+    assert call_fwd(lib, opts=bd._opts(tile_order=2)) == bd.EINVAL
 
 
 def test_empty_problem_is_ok_without_launch(lib):

@@ -173,3 +173,14 @@ def test_grid_size_does_not_change_result():
     b = fused(dq, dk, dv, 2, cfg.scale, grid=3)
     for x, y in zip(a.parts, b.parts):
         assert torch.equal(x.view(torch.int16), y.view(torch.int16))
+
+
+@pytest.mark.parametrize("name", ["image", "tiny"])
+def test_chunk_interleaved_order_gives_identical_output(name):
+    cfg = workloads.CONFIGS[name]
+    _, _, _, dq, dk, dv = cuda_qkv(cfg, seed=8)
+    a = fused(dq, dk, dv, cfg.P, cfg.scale)
+    b = fused(dq, dk, dv, cfg.P, cfg.scale, tile_order=1)
+    assert b.guards_intact()
+    for x, y in zip(a.parts, b.parts):
+        assert torch.equal(x.view(torch.int16), y.view(torch.int16))

@@ -32,6 +32,7 @@ EXPORTED = (
     "attn_a2a_fwd_host",
     "xstage_probe_run",
     "xstage_probe_run_noalloc",
+    "moe_gemm_scatter",
     "attn_a2a_strerror",
     "attn_a2a_num_sms",
 )
@@ -104,6 +105,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.attn_a2a_fwd_host.argtypes = [vp, vp, vp, shp, cint, ctypes.c_float, vp, vp, vp, pp, pp, vp, vp]
     lib.xstage_probe_run.argtypes = [ctypes.POINTER(ProbeCfg), vp]
     lib.xstage_probe_run_noalloc.argtypes = [ctypes.POINTER(ProbeCfg), vp]
+    lib.moe_gemm_scatter.argtypes = [vp, vp, vp, cint, cint, cint, cint, vp, cint, vp, vp, cint, pp,
+                                     ctypes.POINTER(ctypes.c_int), vp, cint, vp]
     lib.attn_a2a_strerror.argtypes = [cint]
     lib.attn_a2a_strerror.restype = ctypes.c_char_p
     lib.attn_a2a_num_sms.argtypes = []
@@ -279,6 +282,24 @@ def xstage_probe_run_noalloc(K: int, rounds: int, V_bytes: int, G_ns: int, stamp
                    None, 0, _ptr(stamps), int(fma_iters))
     rc = lib.xstage_probe_run_noalloc(ctypes.byref(cfg), _stream(stream))
     return _check(rc, "xstage_probe_run_noalloc", check)
+
+
+def moe_gemm_scatter(x, w1, w2, tasks, h_out, row_map, dst, dev_status=None, grid: int = 0, stream=None,
+                     check: bool = True) -> int:
+    """Grouped GEMM task list (kind 0: h_out tile; kind 1: scattered rows into dst[rank])."""
+    lib = load()
+    E, T, K = x.shape
+    N = w1.shape[1]
+    for t in (x, w1, w2, h_out):
+        if t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError("x, w1, w2, h_out must be contiguous bf16")
+    if tasks.dtype != torch.int32 or row_map.dtype != torch.int32:
+        raise ValueError("tasks and row_map must be int32")
+    rows = (ctypes.c_int * len(dst))(*[int(d.shape[0]) for d in dst])
+    rc = lib.moe_gemm_scatter(_ptr(x), _ptr(w1), _ptr(w2), E, T, K, N, _ptr(tasks), int(tasks.shape[0]), _ptr(h_out),
+                              _ptr(row_map), len(dst), _ptr_array(dst), rows, _ptr(dev_status), int(grid),
+                              _stream(stream))
+    return _check(rc, "moe_gemm_scatter", check)
 
 
 def attn_a2a_strerror(code: int) -> str:

@@ -282,6 +282,28 @@ int attn_a2a_fwd_host(const void* hq, const void* hk, const void* hv, const attn
   return ATTN_A2A_OK;
 }
 
+int moe_gemm_scatter(const void* x, const void* w1, const void* w2, int E, int T, int K, int N,
+                     const int* tasks, int n_tasks, void* h_out, const int* row_map, int P,
+                     void* const* dst, const int* dst_rows, int* dev_status, int grid, void* stream) {
+  if (E < 1 || T < 128 || T % 128 != 0 || K < 64 || K % 64 != 0 || N < 128 || N % 128 != 0)
+    return ATTN_A2A_EINVAL;
+  if (static_cast<long long>(E) * T >= (1ll << 31) || static_cast<long long>(E) * T * N >= (1ll << 40))
+    return ATTN_A2A_EUNSUPPORTED;
+  if (n_tasks < 0 || grid < 0 || P < 1 || P > 64 || dst == nullptr || dst_rows == nullptr) return ATTN_A2A_EINVAL;
+  if (n_tasks == 0) return ATTN_A2A_OK;
+  if (x == nullptr || w1 == nullptr || w2 == nullptr || h_out == nullptr || tasks == nullptr || row_map == nullptr)
+    return ATTN_A2A_EINVAL;
+  if (!aligned16(x) || !aligned16(w1) || !aligned16(w2) || !aligned16(h_out) || !aligned16(tasks) ||
+      (reinterpret_cast<uintptr_t>(row_map) & 3u) != 0)
+    return ATTN_A2A_EINVAL;
+  for (int j = 0; j < P; ++j) {
+    if (dst_rows[j] < 0 || dst_rows[j] >= (1 << 24)) return ATTN_A2A_EINVAL;
+    if (dst_rows[j] > 0 && (dst[j] == nullptr || !aligned16(dst[j]))) return ATTN_A2A_EINVAL;
+  }
+  return launch_moe_gemm(x, w1, w2, E, T, K, N, tasks, n_tasks, h_out, row_map, P, dst, dst_rows, dev_status,
+                         grid, static_cast<cudaStream_t>(stream));
+}
+
 int xstage_probe_run(const xstage_probe_cfg* cfg, void* stream) {
   if (cfg == nullptr) return ATTN_A2A_EINVAL;
   const xstage_probe_cfg& c = *cfg;

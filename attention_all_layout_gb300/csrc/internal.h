@@ -35,4 +35,8 @@ int launch_permute(const void* o, const attn_a2a_shape& shp, const EpiParams& ep
 
 int launch_probe(const xstage_probe_cfg& cfg, cudaStream_t stream);
 
+int launch_moe_gemm(const void* x, const void* w1, const void* w2, int E, int T, int K, int N,
+                    const int* tasks, int n_tasks, void* h_out, const int* row_map, int P,
+                    void* const* dst, const int* dst_rows, int* dev_status, int grid, cudaStream_t stream);
+
 }  // namespace attn_a2a

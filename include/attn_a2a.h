@@ -251,6 +251,36 @@ int xstage_probe_run(const xstage_probe_cfg* cfg, void* stream);
 
 int xstage_probe_run_noalloc(const xstage_probe_cfg* cfg, void* stream);
 
+/*
+ * moe_gemm_scatter - synthetic MegaMoE-style workload for the pages'
+ * "reshaping" result ("Key Contributions", MegaMoE: an interleaved scheduler
+ * mixes Linear-1 (compute) and Linear-2 (communication) work across expert
+ * waves so that store bursts get larger gaps). A persistent tcgen05 grouped
+ * GEMM runs a caller-ordered task list; each task is one 128 x 128 output
+ * tile of one expert:
+ *   kind 0 ("Linear-1"): h_out[e, rows, cols] = x[e] w1[e]^T, stored locally;
+ *   kind 1 ("Linear-2"): y = x[e] w2[e]^T, each output row r of expert e
+ *                        scattered to dst[rank][slot, cols] with
+ *                        row_map[e*T + r] = (rank << 24) | slot.
+ * Tasks at neighbouring list positions run at the same time on
+ * neighbouring SMs, so the list order (Expert-Wave: each wave's kind-0 tasks,
+ * then its kind-1 tasks; interleaved: kind-0 tasks of the next wave alternate
+ * with kind-1 tasks of the current one) shapes the store bursts.
+ *   x  : device bf16 [E, T, K]; w1, w2 : device bf16 [E, N, K] (K contiguous).
+ *   T % 128 == 0, K % 64 == 0, N % 128 == 0.
+ *   tasks   : device int32 [n_tasks][4] = (kind, expert, row block, column block).
+ *   h_out   : device bf16 [E, T, N].  row_map : device int32 [E * T].
+ *   dst     : HOST array of P device pointers, dst[j] = bf16 [dst_rows[j], N];
+ *             dst_rows is a HOST array. 1 <= P <= 64.
+ *   grid    : persistent CTAs, 0 = one per SM.
+ * Malformed tasks and out-of-range row_map entries are skipped on the device
+ * and reported as ATTN_A2A_EINVAL through dev_status. Every task writes its
+ * own output tile, so the result does not depend on the order.
+ */
+int moe_gemm_scatter(const void* x, const void* w1, const void* w2, int E, int T, int K, int N,
+                     const int* tasks, int n_tasks, void* h_out, const int* row_map, int P,
+                     void* const* dst, const int* dst_rows, int* dev_status, int grid, void* stream);
+
 /* Static description of a status code. Never NULL. */
 const char* attn_a2a_strerror(int status);
 

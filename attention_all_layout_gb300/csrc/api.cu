@@ -5,6 +5,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "attn_a2a.h"
 #include "internal.h"
@@ -95,6 +96,36 @@ bool partitions_alias_inputs(const attn_a2a_shape& shp, const EpiParams& e, cons
       if (overlaps(out, in[i])) return true;
   }
   return false;
+}
+
+// Copy streams and events of the host-buffer entry point, created once per
+// device on first use (host-side resources; no device memory).
+constexpr int kHostChunks = 4;
+
+struct HostPipe {
+  std::once_flag once;
+  std::mutex mu;
+  bool ok = false;
+  cudaStream_t h2d = nullptr, d2h = nullptr;
+  cudaEvent_t ev_start = nullptr, ev_h2d = nullptr, ev_comp = nullptr, ev_end = nullptr;
+};
+
+HostPipe g_pipes[128];
+
+HostPipe* host_pipe() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return nullptr;
+  HostPipe* hp = &g_pipes[dev];
+  std::call_once(hp->once, [hp] {
+    const unsigned ef = cudaEventDisableTiming;
+    hp->ok = cudaStreamCreateWithFlags(&hp->h2d, cudaStreamNonBlocking) == cudaSuccess &&
+             cudaStreamCreateWithFlags(&hp->d2h, cudaStreamNonBlocking) == cudaSuccess &&
+             cudaEventCreateWithFlags(&hp->ev_start, ef) == cudaSuccess &&
+             cudaEventCreateWithFlags(&hp->ev_h2d, ef) == cudaSuccess &&
+             cudaEventCreateWithFlags(&hp->ev_comp, ef) == cudaSuccess &&
+             cudaEventCreateWithFlags(&hp->ev_end, ef) == cudaSuccess;
+  });
+  return hp->ok ? hp : nullptr;
 }
 
 attn_a2a_opts default_opts() {
@@ -263,22 +294,72 @@ int attn_a2a_fwd_host(const void* hq, const void* hk, const void* hv, const attn
   rc = make_partitions(s, P, dparts, &epi);
   if (rc != ATTN_A2A_OK) return rc;
   if (empty) return ATTN_A2A_OK;
-  const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const size_t bytes = static_cast<size_t>(s.B) * s.H * s.S * s.d * 2u;
-  if (cudaMemcpyAsync(dq, hq, bytes, cudaMemcpyHostToDevice, st) != cudaSuccess ||
-      cudaMemcpyAsync(dk, hk, bytes, cudaMemcpyHostToDevice, st) != cudaSuccess ||
-      cudaMemcpyAsync(dv, hv, bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
-    return ATTN_A2A_ECUDA;
-  rc = fwd_common(dq, dk, dv, &s, P, scale, dparts, nullptr, true, dev_status, nullptr, stream);
-  if (rc != ATTN_A2A_OK) return rc;
-  for (int j = 0; j < P; ++j) {
-    const int c = epi.cbase + (j < epi.crem ? 1 : 0);
-    if (c == 0) continue;
-    if (hparts[j] == nullptr) return ATTN_A2A_EINVAL;
-    const size_t pb = static_cast<size_t>(s.B) * c * s.H * s.d * 2u;
-    if (cudaMemcpyAsync(hparts[j], dparts[j], pb, cudaMemcpyDeviceToHost, st) != cudaSuccess)
-      return ATTN_A2A_ECUDA;
+  for (int j = 0; j < P; ++j)
+    if (epi.cbase + (j < epi.crem ? 1 : 0) > 0 && hparts[j] == nullptr) return ATTN_A2A_EINVAL;
+  {
+    const Span in[3] = {tensor_span(dq, s.B, s.H, s.S, s.d, s.q_sb, s.q_sh, s.q_ss),
+                        tensor_span(dk, s.B, s.H, s.S, s.d, s.k_sb, s.k_sh, s.k_ss),
+                        tensor_span(dv, s.B, s.H, s.S, s.d, s.v_sb, s.v_sh, s.v_ss)};
+    if (partitions_alias_inputs(s, epi, in, 3)) return ATTN_A2A_EINVAL;
   }
+  HostPipe* hp = host_pipe();
+  if (hp == nullptr) return ATTN_A2A_ECUDA;
+  std::lock_guard<std::mutex> lock(hp->mu);
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // Heads are processed in chunks: the host->device copy of the next chunk and
+  // the device->host copy of the previous one overlap the kernel of this one.
+  const int nchunk = s.H < kHostChunks ? s.H : kHostChunks;
+  const int hc = (s.H + nchunk - 1) / nchunk;
+  const size_t head_elems = static_cast<size_t>(s.S) * s.d;
+  // device buffers may still be in use by earlier work on the caller's stream
+  if (cudaEventRecord(hp->ev_start, st) != cudaSuccess || cudaStreamWaitEvent(hp->h2d, hp->ev_start, 0) != cudaSuccess)
+    return ATTN_A2A_ECUDA;
+  const attn_a2a_opts o = default_opts();
+  for (int b = 0; b < s.B; ++b) {
+    for (int h0 = 0; h0 < s.H; h0 += hc) {
+      const int h1 = h0 + hc < s.H ? h0 + hc : s.H;
+      const size_t off = (static_cast<size_t>(b) * s.H + h0) * head_elems;  // elements
+      const size_t bytes = static_cast<size_t>(h1 - h0) * head_elems * 2u;
+      const void* hsrc[3] = {hq, hk, hv};
+      void* ddst[3] = {dq, dk, dv};
+      for (int i = 0; i < 3; ++i)
+        if (cudaMemcpyAsync(static_cast<uint16_t*>(ddst[i]) + off, static_cast<const uint16_t*>(hsrc[i]) + off, bytes,
+                            cudaMemcpyHostToDevice, hp->h2d) != cudaSuccess)
+          return ATTN_A2A_ECUDA;
+      if (cudaEventRecord(hp->ev_h2d, hp->h2d) != cudaSuccess || cudaStreamWaitEvent(st, hp->ev_h2d, 0) != cudaSuccess)
+        return ATTN_A2A_ECUDA;
+      attn_a2a_shape cs = s;  // one batch entry, heads [h0, h1)
+      cs.B = 1;
+      cs.H = h1 - h0;
+      EpiParams ce = epi;
+      ce.hstride = s.H;
+      for (int j = 0; j < P; ++j) {
+        const int c = epi.cbase + (j < epi.crem ? 1 : 0);
+        ce.part[j] = c > 0 ? static_cast<void*>(static_cast<uint16_t*>(dparts[j]) +
+                                                 (static_cast<size_t>(b) * c * s.H + h0) * s.d)
+                           : nullptr;
+      }
+      rc = launch_fa_tc(static_cast<uint16_t*>(dq) + off, static_cast<uint16_t*>(dk) + off,
+                        static_cast<uint16_t*>(dv) + off, cs, scale, true, ce, dev_status, o, st);
+      if (rc != ATTN_A2A_OK) return rc;
+      if (cudaEventRecord(hp->ev_comp, st) != cudaSuccess || cudaStreamWaitEvent(hp->d2h, hp->ev_comp, 0) != cudaSuccess)
+        return ATTN_A2A_ECUDA;
+      for (int j = 0; j < P; ++j) {
+        const int c = epi.cbase + (j < epi.crem ? 1 : 0);
+        if (c == 0) continue;
+        const size_t eoff = (static_cast<size_t>(b) * c * s.H + h0) * s.d;
+        const size_t pitch = static_cast<size_t>(s.H) * s.d * 2u;
+        if (cudaMemcpy2DAsync(static_cast<uint16_t*>(hparts[j]) + eoff, pitch,
+                              static_cast<const uint16_t*>(dparts[j]) + eoff, pitch,
+                              static_cast<size_t>(h1 - h0) * s.d * 2u, c, cudaMemcpyDeviceToHost,
+                              hp->d2h) != cudaSuccess)
+          return ATTN_A2A_ECUDA;
+      }
+    }
+  }
+  // the caller's stream completes only when the last copy back has
+  if (cudaEventRecord(hp->ev_end, hp->d2h) != cudaSuccess || cudaStreamWaitEvent(st, hp->ev_end, 0) != cudaSuccess)
+    return ATTN_A2A_ECUDA;
   return ATTN_A2A_OK;
 }
 

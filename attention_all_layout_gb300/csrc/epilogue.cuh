@@ -17,6 +17,8 @@ struct EpiParams {
   int P;                      // virtual ranks
   int cbase;                  // floor(S / P)
   int crem;                   // S mod P: chunks 0 .. crem-1 hold cbase + 1 rows
+  int hstride;                // heads per partition row when it exceeds the launch's H
+                              // (a launch over a slice of the heads); 0 = H
 };
 
 // Chunk j holding sequence row s, its local row l and its length c_j.
@@ -45,7 +47,8 @@ __device__ __forceinline__ uint16_t* out_row_ptr(const EpiParams& e, int B_unuse
     int j, l, c;
     chunk_of_row(e, s, j, l, c);
     uint16_t* base = static_cast<uint16_t*>(e.part[j]);
-    return base + ((static_cast<int64_t>(b) * c + l) * H + h) * D;
+    const int hs = e.hstride > 0 ? e.hstride : H;
+    return base + ((static_cast<int64_t>(b) * c + l) * hs + h) * D;
   } else {
     uint16_t* base = static_cast<uint16_t*>(e.out);
     return base + ((static_cast<int64_t>(b) * H + h) * S + s) * D;

@@ -174,11 +174,17 @@ int attn_a2a_fwd_simt(const void* q, const void* k, const void* v, const attn_a2
 
 /*
  * attn_a2a_fwd_host - the product call from host memory, for callers whose
- * data lives on the host. On `stream`: copies q, k, v (host, contiguous
- * [B,H,S,d] bf16, pinned for asynchronous copies) into the caller's device
- * buffers dq, dk, dv, runs attn_a2a_fwd into the caller's device partitions
- * dparts[j], then copies each partition back into hparts[j] (host). Returns
- * after enqueueing; synchronise the stream before reading hparts.
+ * data lives on the host: copies q, k, v (host, contiguous [B,H,S,d] bf16,
+ * pinned for asynchronous copies) into the caller's device buffers dq, dk,
+ * dv, runs the fused attention into the caller's device partitions dparts[j],
+ * and copies each partition back into hparts[j] (host). The heads are
+ * processed in up to four chunks so that the copies of one chunk overlap the
+ * kernel of another; the copies run on two library-owned streams (created,
+ * with four events, on the first call per device) ordered by events against
+ * `stream`: they start after the work already queued on `stream`, and
+ * `stream` completes only after the last copy back. Returns after enqueueing;
+ * synchronise `stream` before reading hparts. Calls on one device are
+ * serialised while they enqueue.
  */
 int attn_a2a_fwd_host(const void* hq, const void* hk, const void* hv, const attn_a2a_shape* shp,
                       int P, float scale, void* dq, void* dk, void* dv,

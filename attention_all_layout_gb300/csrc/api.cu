@@ -366,7 +366,7 @@ int attn_a2a_fwd_host(const void* hq, const void* hk, const void* hv, const attn
 int moe_gemm_scatter(const void* x, const void* w1, const void* w2, int E, int T, int K, int N,
                      const int* tasks, int n_tasks, void* h_out, const int* row_map, int P,
                      void* const* dst, const int* dst_rows, int* dev_status, int grid, void* stream) {
-  if (E < 1 || T < 128 || T % 128 != 0 || K < 64 || K % 64 != 0 || N < 128 || N % 128 != 0)
+  if (E < 1 || T < 128 || T % 128 != 0 || K < 64 || K % 64 != 0 || N < 256 || N % 256 != 0)
     return ATTN_A2A_EINVAL;
   if (static_cast<long long>(E) * T >= (1ll << 31) || static_cast<long long>(E) * T * N >= (1ll << 40))
     return ATTN_A2A_EUNSUPPORTED;

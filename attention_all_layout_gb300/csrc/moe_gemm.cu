@@ -13,10 +13,12 @@
 // at the same time on neighbouring SMs.
 //
 // CTA: 256 threads. Warp 0 TMA producer, warp 1 MMA issuer (one thread) and
-// TMEM owner, warps 4-7 epilogue (thread = output row). Tile 128 x 128, K in
-// 64-element steps through a 6-stage shared-memory ring, two TMEM
-// accumulators (256 columns) so the epilogue of one task overlaps the MMAs
-// of the next.
+// TMEM owner, warps 4-7 epilogue (thread = output row). Tile 128 x 256 (one
+// M=128 N=256 MMA per 16-wide K slice: at N=128 the shared-memory operand
+// reads of a 128x128 MMA alone keep the tensor core from its peak), K in
+// 64-element steps through a 4-stage shared-memory ring, two TMEM
+// accumulators (512 columns) so the epilogue of one task overlaps the MMAs
+// of the next; the epilogue drains each accumulator in two 128-column halves.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -30,12 +32,13 @@
 namespace attn_a2a {
 namespace moe {
 
-constexpr int kBM = 128, kBN = 128, kBK = 64;
-constexpr int kStages = 6;
+constexpr int kBM = 128, kBN = 256, kBK = 64;
+constexpr int kHalf = 128;  // accumulator columns the epilogue holds in registers at a time
+constexpr int kStages = 4;
 constexpr int kThreads = 256;
-constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kTmemCols = 512;
 constexpr int kTileBytes = 128 * kBK * 2;       // one 128 x 64 bf16 operand tile (one swizzle atom wide)
-constexpr int kStageBytes = 2 * kTileBytes;     // A and B
+constexpr int kStageBytes = 3 * kTileBytes;     // A and the two 128-row halves of B
 constexpr int kBarOff = kStages * kStageBytes;  // 192 KB
 // barrier slots: FULL[kStages], EMPTY[kStages], AFULL[2], AEMPTY[2], DONE
 constexpr int FULL = 0, EMPTY = kStages, AFULL = 2 * kStages, AEMPTY = 2 * kStages + 2, DONE = 2 * kStages + 4;
@@ -132,6 +135,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t st = sbase + s * kStageBytes;
           tma_load_4d(st, &maps.x, BAR(FULL + s), kc * kBK, t.z * kBM, t.y, 0, pol);
           tma_load_4d(st + kTileBytes, wm, BAR(FULL + s), kc * kBK, t.w * kBN, t.y, 0, pol);
+          tma_load_4d(st + 2 * kTileBytes, wm, BAR(FULL + s), kc * kBK, t.w * kBN + 128, t.y, 0, pol);  // B rows 128..255
         }
       }
       if (!ok) {  // wait (bounded) for the copies already started
@@ -193,11 +197,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool got = __all_sync(0xffffffffu, mbar_wait(BAR(AFULL + ab), (tl >> 1) & 1, w));
       if (!got) break;
       tc_fence_after();
-      uint32_t acc[128];
-      tmem_ld_x128(tmem + lane_off + ab * kBN, acc);
-      tc_fence_before();
-      mbar_arrive(BAR(AEMPTY + ab));  // the accumulator may be reused by the task after next
-      ++tl;
       const int row = t.z * kBM + r;  // row of expert t.y
       uint16_t* dst = nullptr;
       if (t.x == 0) {
@@ -210,10 +209,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         else
           flag_bad_input(p);
       }
-      if (dst != nullptr) {
-        uint4* d4 = reinterpret_cast<uint4*>(dst);
+      for (int half = 0; half < kBN / kHalf; ++half) {
+        uint32_t acc[kHalf];
+        tmem_ld_x128(tmem + lane_off + ab * kBN + half * kHalf, acc);
+        if (half == kBN / kHalf - 1) {  // the whole accumulator is in registers
+          tc_fence_before();
+          mbar_arrive(BAR(AEMPTY + ab));
+        }
+        if (dst == nullptr) continue;
+        uint4* d4 = reinterpret_cast<uint4*>(dst + half * kHalf);
 #pragma unroll
-        for (int c = 0; c < kBN / 8; ++c) {
+        for (int c = 0; c < kHalf / 8; ++c) {
           uint4 v;
           __nv_bfloat162 h0 = __floats2bfloat162_rn(__uint_as_float(acc[8 * c + 0]), __uint_as_float(acc[8 * c + 1]));
           __nv_bfloat162 h1 = __floats2bfloat162_rn(__uint_as_float(acc[8 * c + 2]), __uint_as_float(acc[8 * c + 3]));
@@ -226,6 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           d4[c] = v;
         }
       }
+      ++tl;
     }
   }
   tc_fence_before();

@@ -5,7 +5,7 @@ so every SM stores at the same time; the interleaved scheduler mixes the next
 wave's Linear-1 tiles with the current wave's Linear-2 tiles so that each
 burst of stores has compute behind it.
 
-Task = (kind, expert, row block, column block); kind 0 = Linear-1-like
+Task = (kind, expert, row block, column block) for a 128 x 256 output tile; kind 0 = Linear-1-like
 (output kept), kind 1 = Linear-2-like (output rows scattered to the ranks).
 """
 from __future__ import annotations
@@ -17,9 +17,11 @@ import sys
 import numpy as np
 import torch
 
+TILE_M, TILE_N = 128, 256  # output tile of one task
+
 
 def _wave_tasks(kind, experts, T, N):
-    return [(kind, e, m, n) for e in experts for m in range(T // 128) for n in range(N // 128)]
+    return [(kind, e, m, n) for e in experts for m in range(T // TILE_M) for n in range(N // TILE_N)]
 
 
 def expert_wave_tasks(E: int, T: int, N: int, experts_per_wave: int) -> np.ndarray:
@@ -69,7 +71,7 @@ def time_orders(E=32, T=512, K=1024, N=512, P=8, experts_per_wave=None, reps=20)
     from . import binding as bd
 
     if experts_per_wave is None:  # one wave of Linear-1 tasks fills the GPU about once
-        per_expert = (T // 128) * (N // 128)
+        per_expert = (T // TILE_M) * (N // TILE_N)
         experts_per_wave = max(1, round(bd.num_sms() / per_expert))
     x, w1, w2 = make_inputs(E, T, K, N)
     rm, rows = round_robin_row_map(E, T, P)

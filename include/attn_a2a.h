@@ -262,8 +262,8 @@ int xstage_probe_run_noalloc(const xstage_probe_cfg* cfg, void* stream);
  * "reshaping" result ("Key Contributions", MegaMoE: an interleaved scheduler
  * mixes Linear-1 (compute) and Linear-2 (communication) work across expert
  * waves so that store bursts get larger gaps). A persistent tcgen05 grouped
- * GEMM runs a caller-ordered task list; each task is one 128 x 128 output
- * tile of one expert:
+ * GEMM runs a caller-ordered task list; each task is one 128 x 256 output
+ * tile (128 token rows, 256 output columns) of one expert:
  *   kind 0 ("Linear-1"): h_out[e, rows, cols] = x[e] w1[e]^T, stored locally;
  *   kind 1 ("Linear-2"): y = x[e] w2[e]^T, each output row r of expert e
  *                        scattered to dst[rank][slot, cols] with
@@ -273,8 +273,9 @@ int xstage_probe_run_noalloc(const xstage_probe_cfg* cfg, void* stream);
  * then its kind-1 tasks; interleaved: kind-0 tasks of the next wave alternate
  * with kind-1 tasks of the current one) shapes the store bursts.
  *   x  : device bf16 [E, T, K]; w1, w2 : device bf16 [E, N, K] (K contiguous).
- *   T % 128 == 0, K % 64 == 0, N % 128 == 0.
- *   tasks   : device int32 [n_tasks][4] = (kind, expert, row block, column block).
+ *   T % 128 == 0, K % 64 == 0, N % 256 == 0.
+ *   tasks   : device int32 [n_tasks][4] = (kind, expert, row block, column block):
+ *             rows [128 m, 128 m + 128), columns [256 n, 256 n + 256).
  *   h_out   : device bf16 [E, T, N].  row_map : device int32 [E * T].
  *   dst     : HOST array of P device pointers, dst[j] = bf16 [dst_rows[j], N];
  *             dst_rows is a HOST array. 1 <= P <= 64.

@@ -168,3 +168,20 @@ def test_s2s_validation(lib):
                                 ptrs(200, 2), None, None) == bd.EINVAL
     assert lib.attn_a2a_fwd_s2s(None, ptrs(200, 2), ptrs(300, 2), ctypes.byref(shp), 2, 0.1, ptrs(400, 2),
                                 None, None) == bd.EINVAL
+
+
+def test_moe_validation(lib):
+    dst = (ctypes.c_void_p * 2)(FAKE * 20, FAKE * 21)
+    rows = (ctypes.c_int * 2)(64, 64)
+
+    def run(E=2, T=128, K=128, N=256, n_tasks=4, P=2):
+        return lib.moe_gemm_scatter(FAKE, FAKE * 2, FAKE * 3, E, T, K, N, FAKE * 4, n_tasks, FAKE * 5,
+                                    FAKE * 6, P, dst, rows, None, 0, None)
+
+    assert run(N=128) == bd.EINVAL  # a task is 256 output columns wide
+    assert run(N=384) == bd.EINVAL
+    assert run(T=100) == bd.EINVAL
+    assert run(K=96) == bd.EINVAL
+    assert run(P=0) == bd.EINVAL
+    assert run(n_tasks=-1) == bd.EINVAL
+    assert run(n_tasks=0) == bd.OK  # nothing to do, nothing launched

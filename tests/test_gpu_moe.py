@@ -23,7 +23,7 @@ def run(x, w1, w2, tasks_np, rm, rows, N, status=None):
     return h, dst
 
 
-@pytest.mark.parametrize("E,T,K,N,P,epw", [(4, 256, 256, 256, 4, 2), (3, 384, 128, 128, 2, 2), (6, 128, 512, 384, 8, 4)])
+@pytest.mark.parametrize("E,T,K,N,P,epw", [(4, 256, 256, 256, 4, 2), (3, 384, 128, 256, 2, 2), (6, 128, 512, 768, 8, 4)])
 def test_moe_matches_oracle_both_orders(E, T, K, N, P, epw):
     x, w1, w2 = ms.make_inputs(E, T, K, N, seed=E + K, device="cpu")
     xd, w1d, w2d = x.cuda(), w1.cuda(), w2.cuda()
@@ -42,7 +42,7 @@ def test_moe_matches_oracle_both_orders(E, T, K, N, P, epw):
 
 
 def test_malformed_tasks_and_row_map_are_flagged_and_skipped():
-    E, T, K, N, P = 2, 128, 128, 128, 2
+    E, T, K, N, P = 2, 128, 128, 256, 2
     x, w1, w2 = ms.make_inputs(E, T, K, N, seed=3, device="cpu")
     rm, rows = ms.round_robin_row_map(E, T, P)
     tasks = ms.expert_wave_tasks(E, T, N, 2)

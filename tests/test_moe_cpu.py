@@ -10,18 +10,20 @@ from oracle import moe as om
 
 def test_orders_hold_the_same_tasks():
     for E, epw in ((8, 2), (5, 3), (4, 4)):
-        a = ms.expert_wave_tasks(E, 256, 256, epw)
-        b = ms.interleaved_tasks(E, 256, 256, epw)
+        a = ms.expert_wave_tasks(E, 256, 512, epw)
+        b = ms.interleaved_tasks(E, 256, 512, epw)
         assert a.shape == b.shape == (E * 2 * 2 * 2, 4)
         assert sorted(map(tuple, a)) == sorted(map(tuple, b))
         assert len(set(map(tuple, a))) == len(a)
 
 
 def test_expert_wave_groups_kinds_and_interleaved_alternates():
-    a = ms.expert_wave_tasks(4, 128, 128, 2)
+    a = ms.expert_wave_tasks(4, 128, 256, 2)
     assert [int(t[0]) for t in a] == [0, 0, 1, 1, 0, 0, 1, 1]
-    b = ms.interleaved_tasks(4, 128, 128, 2)
+    b = ms.interleaved_tasks(4, 128, 256, 2)
     assert [(int(t[0]), int(t[1])) for t in b] == [(0, 0), (0, 1), (1, 0), (0, 2), (1, 1), (0, 3), (1, 2), (1, 3)]
+    # tasks are 128 x 256 output tiles: N = 768 gives column blocks 0..2
+    assert sorted({int(t[3]) for t in ms.expert_wave_tasks(1, 128, 768, 1)}) == [0, 1, 2]
 
 
 def test_round_robin_row_map():
@@ -39,7 +41,7 @@ def brute(x, w1, w2, tasks, rm, rows):
     for kind, e, m, n in tasks.tolist():
         w = w1 if kind == 0 else w2
         for r in range(128 * m, 128 * m + 128):
-            for c in range(128 * n, 128 * n + 128):
+            for c in range(256 * n, 256 * n + 256):
                 acc = sum(float(x[e, r, k]) * float(w[e, c, k]) for k in range(K))
                 if kind == 0:
                     h[e][r][c] = acc
@@ -51,7 +53,7 @@ def brute(x, w1, w2, tasks, rm, rows):
 
 def test_oracle_against_brute_force():
     g = torch.Generator().manual_seed(0)
-    E, T, K, N, P = 2, 128, 3, 128, 2
+    E, T, K, N, P = 2, 128, 3, 256, 2
     x = torch.randn((E, T, K), generator=g).to(torch.bfloat16)
     w1 = torch.randn((E, N, K), generator=g).to(torch.bfloat16)
     w2 = torch.randn((E, N, K), generator=g).to(torch.bfloat16)
@@ -65,7 +67,7 @@ def test_oracle_against_brute_force():
 
 
 def test_oracle_identity_and_one_hot_weights():
-    E, T, K, N, P = 1, 128, 128, 128, 4
+    E, T, K, N, P = 1, 128, 256, 256, 4
     x = torch.randn((E, T, K), generator=torch.Generator().manual_seed(1)).to(torch.bfloat16)
     eye = torch.eye(K).reshape(1, N, K).to(torch.bfloat16)
     tasks = ms.expert_wave_tasks(E, T, N, 1)

@@ -47,7 +47,11 @@ constexpr int kBM = 128;  // query rows per tile
 constexpr int kBN = 128;  // keys per block
 constexpr int kThreads = 384;
 constexpr uint32_t kTmemCols = 512;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units: keep a stale row max until it lags by 2^8
+// A block's probabilities are taken against the row's running maximum m as
+// long as their sum stays within kSpecBound (then no single p exceeds it and
+// the fp32 accumulators stay far from overflow); past it the block's own
+// maximum is taken and O and l are rescaled.
+constexpr float kSpecBound = 4096.0f;  // 2^12
 // Every kPolyEvery-th pair of probabilities is exponentiated on the FMA pipe
 // (exp2_poly_x2) instead of the MUFU; 0 = all on the MUFU. Off: GB300's MUFU
 // keeps up with the softmax here, and moving 1/8, 1/4 or 1/2 of the pairs to
@@ -384,14 +388,21 @@ __device__ void softmax_role(const Params& p, int t, uint32_t bar0, uint32_t tme
       tmem_ld_x128(tS, sr);
       const Blk bk = locate_block<MODE>(p, j);
       const int valid = bk.c - bk.row;  // keys of this block that exist (>= 128 except at the end)
-      const float mx = valid >= kBN ? row_max<false>(sr, valid) : row_max<true>(sr, valid);
-      const float m_new = mx * sl2;
-      // Lazy rescaling: keep a stale row maximum until some row of the warp
-      // has moved more than 2^8 past it. The decision is warp-uniform because
-      // the TMEM loads and stores below are warp-collective; rows whose
-      // maximum did not grow get alpha = 2^0 = 1 exactly.
-      if (__any_sync(0xffffffffu, m_new > m_used + kRescaleThreshold)) {
-        const float m_tgt = fmaxf(m_used, m_new);
+      uint32_t pk[64];
+      // Exponentiate against the running maximum m_used without first taking
+      // this block's maximum (the maximum only guards against overflow, and
+      // it moves rarely once a few blocks are in). Every p is at most the
+      // block's row sum, so a sum within kSpecBound proves the stale maximum
+      // safe; otherwise (and on the first block) take the block's maximum,
+      // rescale O and l by 2^(m_used - m_new), and redo the block. The
+      // decision is warp-uniform because the TMEM loads and stores are
+      // warp-collective; rows whose maximum did not grow get alpha = 1.
+      float ls = -1.0f;
+      if (m_used != -INFINITY)
+        ls = valid >= kBN ? probs<false>(sr, pk, sl2, -m_used, valid) : probs<true>(sr, pk, sl2, -m_used, valid);
+      if (__any_sync(0xffffffffu, !(ls >= 0.0f && ls <= kSpecBound))) {
+        const float mx = valid >= kBN ? row_max<false>(sr, valid) : row_max<true>(sr, valid);
+        const float m_tgt = fmaxf(m_used, mx * sl2);
         // 0 on the first block (m_used = -inf); exactly 1 where the maximum did not move
         const float alpha = m_tgt == m_used ? 1.0f : ex2_approx(m_used - m_tgt);
         if (j > 0) {
@@ -412,9 +423,9 @@ __device__ void softmax_role(const Params& p, int t, uint32_t bar0, uint32_t tme
         }
         l *= alpha;
         m_used = m_tgt;
+        ls = valid >= kBN ? probs<false>(sr, pk, sl2, -m_used, valid) : probs<true>(sr, pk, sl2, -m_used, valid);
       }
-      uint32_t pk[64];
-      l += valid >= kBN ? probs<false>(sr, pk, sl2, -m_used, valid) : probs<true>(sr, pk, sl2, -m_used, valid);
+      l += ls;
       tmem_st_x64(tS, pk);
       tc_fence_before();
       if (!(p.inject_stall && t == 0 && j == 0 && it == 0)) mbar_arrive(BAR(C::PF + t));  // test hook

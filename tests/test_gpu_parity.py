@@ -184,3 +184,24 @@ def test_chunk_interleaved_order_gives_identical_output(name):
     assert b.guards_intact()
     for x, y in zip(a.parts, b.parts):
         assert torch.equal(x.view(torch.int16), y.view(torch.int16))
+
+
+def test_growing_and_jumping_scores_take_the_rescale_path():
+    # Key magnitudes grow along the sequence, so the running row maximum is
+    # overtaken again and again; one block in the middle has scores large
+    # enough that exponentiating it against the stale maximum overflows. Both
+    # force the kernel's fallback (take the block maximum, rescale O and l).
+    B, H, S, d, P = 1, 2, 1536, 128, 2
+    gen = torch.Generator().manual_seed(9)
+    q = torch.randn((B, H, S, d), generator=gen)
+    growth = 1.0 + 6.0 * torch.arange(S, dtype=torch.float32) / S
+    k = torch.randn((B, H, S, d), generator=gen) * growth[None, None, :, None]
+    k[:, :, 700:760] *= 6.0
+    v = torch.randn((B, H, S, d), generator=gen)
+    q, k, v = (t.to(torch.bfloat16) for t in (q, k, v))
+    scale = 1 / math.sqrt(d)
+    g = fused(q.cuda(), k.cuda(), v.cuda(), P, scale)
+    assert g.guards_intact()
+    want = orc.head_to_seq_partitions(orc.attention_fp64(q, k, v, scale), P)
+    for j, (got, w) in enumerate(zip(g.parts, want)):
+        compare(orc.as_f64(got), w, f"growing scores, partition {j}")

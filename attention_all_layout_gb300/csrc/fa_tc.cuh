@@ -13,7 +13,9 @@
 //   warp 0      TMA producer: Q tiles once per work item, then K_j, V_j
 //               through a ring of shared-memory stages
 //   warp 1      MMA issuer (one thread) and TMEM allocator
-//   warps 2-3   idle
+//   warp 2      relay: waits on the TMA, P-ready and O-free barriers on the
+//               issuer's behalf and hands it one event per group of MMAs
+//   warp 3      idle
 //   warps 4-7   softmax/correction/epilogue for query tile 0 (128 rows)
 //   warps 8-11  the same for query tile 1
 // A work item is (b, h, pair of adjacent 128-row query blocks), so each K/V
@@ -29,6 +31,14 @@
 // thread complete in order, the commit after S_t_j also means that the
 // previous P_t V product is done, so the softmax role may rescale O_t in
 // place before it publishes P_t_j.
+//
+// Why a relay: on GB300 any shared-memory load or mbarrier query in the
+// thread that issues tcgen05.mma stalls it behind its queued MMAs (~170-220
+// cycles; measured with back-to-back 128x128x16 MMAs, which run at 64 cycles
+// each undisturbed). The issuer therefore syncs only where the data
+// dependencies force it - before S0_j (K_j landed), before O1 += P1 V (P1
+// ready) and before O0 += P0 V (V_j landed and P0 ready, one event) - and the
+// relay thread does the individual barrier waits.
 #pragma once
 
 #include <cuda.h>
@@ -85,6 +95,8 @@ struct Cfg {
   static constexpr int DONE = KVE + NSTAGE;
   static constexpr int NBAR = DONE + 1;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
+  // MISC: +0 abort flag, +4 TMEM base, +8 relay event count
+  static constexpr int CNT_EV = MISC_OFF + 8;
   static constexpr int SMEM_USED = MISC_OFF + 16;
   static constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack for 1024-byte alignment
 };
@@ -238,10 +250,10 @@ __device__ void mma_role(const Params& p, uint32_t sbase, uint32_t bar0, uint32_
   auto BAR = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
   constexpr uint32_t kIdescQK = idesc_bf16_f32(kBM, kBN, false, false);  // Q, K both K-major
   constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, D, false, true);     // V is MN-major (d contiguous)
+  const uint32_t cnt_ev = sbase + C::CNT_EV;
   uint32_t kv_it = 0;
-  uint32_t pf_cnt[2] = {0, 0};
+  uint32_t ev = 0;
   bool ok = true;
-  int it = 0;
 
   auto issue_qk = [&](int t, uint32_t sK) {
     const uint32_t qa = sbase + C::Q_OFF + t * C::TILE_BYTES;
@@ -253,12 +265,8 @@ __device__ void mma_role(const Params& p, uint32_t sbase, uint32_t bar0, uint32_
               kIdescQK, kk > 0 ? 1u : 0u);
     }
   };
-  // O_t (+)= P_t V_j. Returns false on abort.
-  auto issue_pv = [&](int t, int j, uint32_t sV) -> bool {
-    if (!mbar_wait(BAR(C::PF + t), pf_cnt[t] & 1, w)) return false;
-    ++pf_cnt[t];
-    if (j == 0 && !mbar_wait(BAR(C::OE + t), (it & 1) ^ 1, w)) return false;
-    tc_fence_after();
+  // O_t (+)= P_t V_j; the relay has already seen P_t ready and O_t free.
+  auto issue_pv = [&](int t, int j, uint32_t sV) {
     const uint32_t vb = sbase + C::KV_OFF + sV * C::TILE_BYTES;
 #pragma unroll
     for (int kk = 0; kk < kBN / 16; ++kk) {
@@ -268,21 +276,24 @@ __device__ void mma_role(const Params& p, uint32_t sbase, uint32_t bar0, uint32_
     }
     if (t == 1) umma_commit(BAR(C::KVE + sV));  // V_j now read by both tiles
     if (j == p.nblk - 1) umma_commit(BAR(C::OF + t));
+  };
+  auto sync = [&]() -> bool {
+    if (!counter_wait(cnt_ev, ++ev, w)) return false;
+    tc_fence_after();
     return true;
   };
 
-  for (int item = blockIdx.x; ok && item < p.total; item += gridDim.x, ++it) {
-    ok = mbar_wait(BAR(C::QF + 0), it & 1, w) && mbar_wait(BAR(C::QF + 1), it & 1, w);
-    if (!ok) break;
-    tc_fence_after();
+  for (int item = blockIdx.x; ok && item < p.total; item += gridDim.x) {
     uint32_t sVprev = 0;
     for (int j = 0; j < p.nblk; ++j) {
       const uint32_t sK = kv_it % C::NSTAGE;
-      if (!mbar_wait(BAR(C::KVF + sK), (kv_it / C::NSTAGE) & 1, w)) { ok = false; break; }
-      tc_fence_after();
+      if (!sync()) { ok = false; break; }  // A_j: K_j (and Q at j = 0)
       issue_qk(0, sK);
       umma_commit(BAR(C::SF + 0));
-      if (j > 0 && !issue_pv(1, j - 1, sVprev)) { ok = false; break; }
+      if (j > 0) {
+        if (!sync()) { ok = false; break; }  // C_j: P1_{j-1} (and O1 free at j = 1)
+        issue_pv(1, j - 1, sVprev);
+      }
       issue_qk(1, sK);
       umma_commit(BAR(C::SF + 1));
       umma_commit(BAR(C::KVE + sK));  // K_j read by both tiles
@@ -292,17 +303,63 @@ __device__ void mma_role(const Params& p, uint32_t sbase, uint32_t bar0, uint32_
       }
       ++kv_it;
       const uint32_t sV = kv_it % C::NSTAGE;
-      if (!mbar_wait(BAR(C::KVF + sV), (kv_it / C::NSTAGE) & 1, w)) { ok = false; break; }
-      if (!issue_pv(0, j, sV)) { ok = false; break; }
+      if (!sync()) { ok = false; break; }  // B_j: V_j, P0_j (and O0 free at j = 0)
+      issue_pv(0, j, sV);
       sVprev = sV;
       ++kv_it;
     }
-    if (ok && !issue_pv(1, p.nblk - 1, sVprev)) ok = false;
+    if (ok && !sync()) ok = false;  // E: P1 of the last block (and O1 free if there is one block)
+    if (ok) issue_pv(1, p.nblk - 1, sVprev);
   }
   if (!ok) {
     // Aborting: let every MMA already issued finish before TMEM is freed.
     umma_commit(BAR(C::DONE));
     mbar_wait_drain(BAR(C::DONE), 0, 100000000ull);
+  }
+}
+
+// ------------------------------------------------------------------ relay
+// Does the MMA issuer's fine-grained waits (TMA barriers, P ready, O free)
+// in its issue order and publishes one event per group of MMAs that may go:
+//   A_j  K_j landed (and both Q tiles at j = 0)            -> S0_j
+//   C_j  P1_{j-1} ready (and O1 free at j = 1), j > 0      -> O1 += P1 V, S1_j
+//   B_j  V_j landed and P0_j ready (and O0 free at j = 0)  -> O0 += P0 V
+//   E    P1 of the last block ready (and O1 free if one block) -> last O1 += P1 V
+// Each wait depends only on MMAs issued before the event it gates, and the
+// softmax roles cannot run a barrier two phases ahead of these parity waits
+// (their next phase needs an S that is only issued after the relay's event).
+template <int D>
+__device__ void relay_role(const Params& p, uint32_t sbase, uint32_t bar0, const WaitCtl& w) {
+  using C = Cfg<D>;
+  auto BAR = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
+  const uint32_t cnt_ev = sbase + C::CNT_EV;
+  uint32_t kv_it = 0, ev = 0;
+  uint32_t pf_cnt[2] = {0, 0};
+  int it = 0;
+  auto kv_ready = [&]() -> bool {
+    const bool r = mbar_wait(BAR(C::KVF + kv_it % C::NSTAGE), (kv_it / C::NSTAGE) & 1, w);
+    ++kv_it;
+    return r;
+  };
+  auto p_ready = [&](int t) -> bool { return mbar_wait(BAR(C::PF + t), pf_cnt[t]++ & 1, w); };
+  auto o_free = [&](int t) -> bool { return mbar_wait(BAR(C::OE + t), (it & 1) ^ 1, w); };
+  for (int item = blockIdx.x; item < p.total; item += gridDim.x, ++it) {
+    for (int j = 0; j < p.nblk; ++j) {
+      if (j == 0 && !(mbar_wait(BAR(C::QF + 0), it & 1, w) && mbar_wait(BAR(C::QF + 1), it & 1, w))) return;
+      if (!kv_ready()) return;
+      st_release_u32(cnt_ev, ++ev);  // A_j
+      if (j > 0) {
+        if (!p_ready(1)) return;
+        if (j == 1 && !o_free(1)) return;
+        st_release_u32(cnt_ev, ++ev);  // C_j
+      }
+      if (!kv_ready() || !p_ready(0)) return;
+      if (j == 0 && !o_free(0)) return;
+      st_release_u32(cnt_ev, ++ev);  // B_j
+    }
+    if (!p_ready(1)) return;
+    if (p.nblk == 1 && !o_free(1)) return;
+    st_release_u32(cnt_ev, ++ev);  // E
   }
 }
 
@@ -498,6 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(BAR(C::DONE), 1);
     *abort_flag = 0;
+    reinterpret_cast<uint32_t*>(sgen + C::MISC_OFF)[2] = 0;  // relay event count
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -524,6 +582,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) producer_role<D, MODE, NMAP>(p, &maps, sbase, bar0, w);
     } else if (warp == 1) {
       if (lane == 0) mma_role<D>(p, sbase, bar0, tmem, w);
+    } else if (warp == 2) {
+      if (lane == 0) relay_role<D>(p, sbase, bar0, w);
     }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));

@@ -27,7 +27,8 @@
 //
 // MMA order per key block j (skewed so each softmax has two MMAs of slack):
 //   S0_j = Q0 K_j^T ; O1 += P1_{j-1} V_{j-1} ; S1_j = Q1 K_j^T ; O0 += P0_j V_j
-// and a final O1 += P1 V after the loop. Because tcgen05 operations of one
+// and a final O1 += P1 V after the loop (S0_{j+1} follows O0 += P0_j V_j
+// directly, in the same issue group). Because tcgen05 operations of one
 // thread complete in order, the commit after S_t_j also means that the
 // previous P_t V product is done, so the softmax role may rescale O_t in
 // place before it publishes P_t_j.
@@ -35,10 +36,10 @@
 // Why a relay: on GB300 any shared-memory load or mbarrier query in the
 // thread that issues tcgen05.mma stalls it behind its queued MMAs (~170-220
 // cycles; measured with back-to-back 128x128x16 MMAs, which run at 64 cycles
-// each undisturbed). The issuer therefore syncs only where the data
-// dependencies force it - before S0_j (K_j landed), before O1 += P1 V (P1
-// ready) and before O0 += P0 V (V_j landed and P0 ready, one event) - and the
-// relay thread does the individual barrier waits.
+// each undisturbed). The issuer therefore syncs twice per key block - before
+// O1 += P1 V (P1 ready), and before O0 += P0 V together with the next S0
+// (V_j landed, P0 ready and K_{j+1} landed, one event) - and the relay thread
+// does the individual barrier waits.
 #pragma once
 
 #include <cuda.h>
@@ -285,11 +286,11 @@ __device__ void mma_role(const Params& p, uint32_t sbase, uint32_t bar0, uint32_
 
   for (int item = blockIdx.x; ok && item < p.total; item += gridDim.x) {
     uint32_t sVprev = 0;
+    if (!sync()) { ok = false; break; }  // A: both Q tiles and K_0
+    issue_qk(0, kv_it % C::NSTAGE);
+    umma_commit(BAR(C::SF + 0));
     for (int j = 0; j < p.nblk; ++j) {
       const uint32_t sK = kv_it % C::NSTAGE;
-      if (!sync()) { ok = false; break; }  // A_j: K_j (and Q at j = 0)
-      issue_qk(0, sK);
-      umma_commit(BAR(C::SF + 0));
       if (j > 0) {
         if (!sync()) { ok = false; break; }  // C_j: P1_{j-1} (and O1 free at j = 1)
         issue_pv(1, j - 1, sVprev);
@@ -303,10 +304,16 @@ __device__ void mma_role(const Params& p, uint32_t sbase, uint32_t bar0, uint32_
       }
       ++kv_it;
       const uint32_t sV = kv_it % C::NSTAGE;
-      if (!sync()) { ok = false; break; }  // B_j: V_j, P0_j (and O0 free at j = 0)
+      // B_j: V_j and P0_j (and O0 free at j = 0), and K_{j+1}, so that
+      // O0 += P0 V_j and S0_{j+1} go to the tensor core back to back
+      if (!sync()) { ok = false; break; }
       issue_pv(0, j, sV);
       sVprev = sV;
       ++kv_it;
+      if (j + 1 < p.nblk) {
+        issue_qk(0, kv_it % C::NSTAGE);
+        umma_commit(BAR(C::SF + 0));
+      }
     }
     if (ok && !sync()) ok = false;  // E: P1 of the last block (and O1 free if there is one block)
     if (ok) issue_pv(1, p.nblk - 1, sVprev);
@@ -321,9 +328,10 @@ __device__ void mma_role(const Params& p, uint32_t sbase, uint32_t bar0, uint32_
 // ------------------------------------------------------------------ relay
 // Does the MMA issuer's fine-grained waits (TMA barriers, P ready, O free)
 // in its issue order and publishes one event per group of MMAs that may go:
-//   A_j  K_j landed (and both Q tiles at j = 0)            -> S0_j
-//   C_j  P1_{j-1} ready (and O1 free at j = 1), j > 0      -> O1 += P1 V, S1_j
-//   B_j  V_j landed and P0_j ready (and O0 free at j = 0)  -> O0 += P0 V
+//   A    both Q tiles and K_0 landed (once per item)         -> S0_0
+//   C_j  P1_{j-1} ready (and O1 free at j = 1), j > 0        -> O1 += P1 V, S1_j
+//   B_j  V_j landed, P0_j ready (and O0 free at j = 0), and
+//        K_{j+1} landed unless j is the last block           -> O0 += P0 V, S0_{j+1}
 //   E    P1 of the last block ready (and O1 free if one block) -> last O1 += P1 V
 // Each wait depends only on MMAs issued before the event it gates, and the
 // softmax roles cannot run a barrier two phases ahead of these parity waits
@@ -344,17 +352,18 @@ __device__ void relay_role(const Params& p, uint32_t sbase, uint32_t bar0, const
   auto p_ready = [&](int t) -> bool { return mbar_wait(BAR(C::PF + t), pf_cnt[t]++ & 1, w); };
   auto o_free = [&](int t) -> bool { return mbar_wait(BAR(C::OE + t), (it & 1) ^ 1, w); };
   for (int item = blockIdx.x; item < p.total; item += gridDim.x, ++it) {
+    if (!(mbar_wait(BAR(C::QF + 0), it & 1, w) && mbar_wait(BAR(C::QF + 1), it & 1, w))) return;
+    if (!kv_ready()) return;
+    st_release_u32(cnt_ev, ++ev);  // A
     for (int j = 0; j < p.nblk; ++j) {
-      if (j == 0 && !(mbar_wait(BAR(C::QF + 0), it & 1, w) && mbar_wait(BAR(C::QF + 1), it & 1, w))) return;
-      if (!kv_ready()) return;
-      st_release_u32(cnt_ev, ++ev);  // A_j
       if (j > 0) {
         if (!p_ready(1)) return;
         if (j == 1 && !o_free(1)) return;
         st_release_u32(cnt_ev, ++ev);  // C_j
       }
-      if (!kv_ready() || !p_ready(0)) return;
+      if (!kv_ready() || !p_ready(0)) return;  // V_j, P0_j
       if (j == 0 && !o_free(0)) return;
+      if (j + 1 < p.nblk && !kv_ready()) return;  // K_{j+1}
       st_release_u32(cnt_ev, ++ev);  // B_j
     }
     if (!p_ready(1)) return;

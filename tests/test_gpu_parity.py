@@ -37,6 +37,10 @@ FULL_CASES = [
     ("one_row", 1, 1, 1, 128, 1),
     ("S_lt_P", 1, 8, 5, 64, 8),
     ("one_tile_plus_one", 1, 1, 129, 64, 1),
+    # the partition maximum: 64 ranks of 10-11 rows, so every 128-row tile
+    # straddles a dozen destination partitions
+    ("P64_max_partitions", 1, 64, 700, 64, 64),
+    ("batch3_ragged", 3, 4, 333, 128, 4),
 ]
 
 

@@ -167,6 +167,48 @@ __device__ __forceinline__ Blk locate_block(const Params& p, int idx) {
   return r;
 }
 
+// The key blocks in order, without the division locate_block needs: the
+// softmax and the producer visit blocks 0, 1, 2, ... of every item, and in the
+// sequence-sharded mode a runtime division per block costs the softmax (whose
+// warps keep their sub-partitions busy) several percent.
+template <int MODE>
+struct BlockWalker {
+  int k = 0, b = 0, nbk = 0, ck = 0;  // partition, block in it, its blocks, its rows
+  __device__ __forceinline__ void reset(const Params& p) {
+    k = 0;
+    b = 0;
+    if constexpr (MODE == kModeS2S) {
+      ck = p.epi.crem > 0 ? p.epi.cbase + 1 : p.epi.cbase;
+      nbk = p.epi.crem > 0 ? p.nb_big : p.nb_small;
+    }
+  }
+  __device__ __forceinline__ Blk block(const Params& p) const {
+    Blk r;
+    if constexpr (MODE == kModeS2S) {
+      r.map = k;
+      r.row = b * kBM;
+      r.c = ck;
+    } else {
+      r.map = 0;
+      r.row = b * kBM;
+      r.c = p.S;
+    }
+    return r;
+  }
+  __device__ __forceinline__ void next(const Params& p) {
+    ++b;
+    if constexpr (MODE == kModeS2S) {
+      if (b == nbk) {  // partitions without rows only follow the last block
+        b = 0;
+        if (++k == p.epi.crem) {
+          ck = p.epi.cbase;
+          nbk = p.nb_small;
+        }
+      }
+    }
+  }
+};
+
 struct Item {
   int b, h, pair;
 };
@@ -213,8 +255,10 @@ __device__ void producer_role(const Params& p, const Maps<NMAP>* maps, uint32_t 
       ++q_loads[t];
       return true;
     };
-    auto load_kv = [&](bool is_v, int j) -> bool {
-      const Blk bk = locate_block<MODE>(p, j);
+    BlockWalker<MODE> kw;
+    kw.reset(p);
+    auto load_kv = [&](bool is_v) -> bool {  // the walker's current key block
+      const Blk bk = kw.block(p);
       const CUtensorMap* m = is_v ? &maps->v[bk.map] : &maps->k[bk.map];
       const uint32_t s = kv_it % C::NSTAGE;
       const uint32_t ph = (kv_it / C::NSTAGE) & 1;
@@ -227,8 +271,9 @@ __device__ void producer_role(const Params& p, const Maps<NMAP>* maps, uint32_t 
       ++kv_it;
       return true;
     };
-    ok = load_q(0) && load_kv(false, 0) && load_q(1) && load_kv(true, 0);
-    for (int j = 1; ok && j < p.nblk; ++j) ok = load_kv(false, j) && load_kv(true, j);
+    ok = load_q(0) && load_kv(false) && load_q(1) && load_kv(true);
+    kw.next(p);
+    for (int j = 1; ok && j < p.nblk; ++j, kw.next(p)) ok = load_kv(false) && load_kv(true);
   }
   if (!ok) {
     // Aborting: wait (bounded) for the copies this thread started, so none
@@ -445,6 +490,8 @@ __device__ void softmax_role(const Params& p, int t, uint32_t bar0, uint32_t tme
     const int srow = (2 * wi.pair + t) * kBM + r;
     float m_used = -INFINITY;
     float l = 0.f;
+    BlockWalker<MODE> kb;
+    kb.reset(p);
     for (int j = 0; j < p.nblk; ++j) {
       const bool got = __all_sync(0xffffffffu, mbar_wait(BAR(C::SF + t), sf_cnt & 1, w));
       if (!got) return;
@@ -452,7 +499,8 @@ __device__ void softmax_role(const Params& p, int t, uint32_t bar0, uint32_t tme
       tc_fence_after();
       uint32_t sr[128];
       tmem_ld_x128(tS, sr);
-      const Blk bk = locate_block<MODE>(p, j);
+      const Blk bk = kb.block(p);
+      kb.next(p);
       const int valid = bk.c - bk.row;  // keys of this block that exist (>= 128 except at the end)
       uint32_t pk[64];
       // Exponentiate against the running maximum m_used without first taking

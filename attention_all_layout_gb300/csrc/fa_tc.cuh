@@ -72,7 +72,7 @@ constexpr float kSpecBound = 4096.0f;  // 2^12
 #endif
 constexpr int kPolyEvery = ATTN_A2A_POLY_EVERY;
 // Register split (setmaxnreg): the kernel launches with kLaunchRegs per thread;
-// warpgroup 0 (producer, MMA issuer, two idle warps) gives registers back and
+// warpgroup 0 (producer, MMA issuer, relay, one idle warp) gives registers back and
 // the two softmax warpgroups take them: 128*kRegsLow + 256*kRegsHigh must not
 // exceed 384*kLaunchRegs, else setmaxnreg.inc would wait forever. The launcher
 // refuses to launch unless the compiled launch register count is kLaunchRegs.

@@ -140,11 +140,12 @@ int fwd_common(const void* q, const void* k, const void* v, const attn_a2a_shape
   bool empty = false;
   int rc = check_inputs(q, k, v, shp, scale, &empty);
   if (rc != ATTN_A2A_OK) return rc;
-  if (opts != nullptr && (opts->store_kind < 0 || opts->store_kind > 1 || opts->grid < 0 ||
+  if (opts != nullptr && (opts->store_kind < 0 || opts->store_kind > 2 || opts->grid < 0 ||
                           opts->timeout_ns < 0 || opts->inject_stall < 0 || opts->inject_stall > 1 ||
                           opts->tile_order < 0 || opts->tile_order > 1))
     return ATTN_A2A_EINVAL;
-  if (opts != nullptr && opts->store_kind != 0) return ATTN_A2A_EUNSUPPORTED;  // bulk epilogue not built
+  // the bulk-store epilogue exists for the all-to-all layout with up to 8 partitions
+  if (opts != nullptr && opts->store_kind == 1 && (!a2a || P > 8)) return ATTN_A2A_EUNSUPPORTED;
   EpiParams epi;
   std::memset(&epi, 0, sizeof(epi));
   if (a2a) {

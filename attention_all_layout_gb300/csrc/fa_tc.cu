@@ -52,10 +52,29 @@ bool make_map(CUtensorMap* m, const void* base, int B, int H, int S, int d, long
   return r == CUDA_SUCCESS;
 }
 
+// Output partition j, [B, c_j, H_row, d] bf16 contiguous, addressed as
+// (d, head, row, batch) with heads [0, H) of a row of H_row heads; box of 64
+// columns x 1 head x 128 rows, 128-byte swizzle (the staging buffer's
+// layout). Rows past c_j are not written by a store.
+bool make_out_map(CUtensorMap* m, void* base, int B, int H, int H_row, int c, int d) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(c),
+                        static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(H_row) * d * 2,
+                           static_cast<cuuint64_t>(c) * H_row * d * 2};
+  cuuint32_t box[4] = {64, 1, 128, 1};
+  cuuint32_t estride[4] = {1, 1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims, strides, box, estride,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 template <int D, int MODE, int NMAP>
 int launch_t(const tc::Maps<NMAP>& maps, const tc::Params& p, int grid, cudaStream_t stream) {
   auto kern = tc::fa_fwd_tc_kernel<D, MODE, NMAP>;
-  constexpr int smem = tc::Cfg<D>::SMEM_ALLOC;
+  constexpr int smem = MODE == tc::kModeA2AT ? tc::Cfg<D>::SMEM_ALLOC_STG : tc::Cfg<D>::SMEM_ALLOC;
   // The in-kernel register split assumes exactly this launch register count;
   // with fewer registers at launch the softmax warpgroups could never obtain
   // their share, so refuse to launch rather than risk a stuck kernel.
@@ -92,6 +111,21 @@ int launch_fa_tc(const void* q, const void* k, const void* v, const attn_a2a_sha
                  float scale, bool a2a, const EpiParams& epi, int* dev_status,
                  const attn_a2a_opts& opts, cudaStream_t stream) {
   tc::Maps<1> maps;
+  std::memset(&maps, 0, sizeof(maps));
+  // store_kind 0: bulk tensor stores where they are built (the all-to-all
+  // layout with up to kMaxStoreMaps partitions), else row stores; 1: bulk
+  // stores or EUNSUPPORTED; 2: row stores from registers
+  const bool bulk_ok = a2a && epi.P <= tc::kMaxStoreMaps;
+  if (opts.store_kind == 1 && !bulk_ok) return ATTN_A2A_EUNSUPPORTED;
+  const bool bulk = bulk_ok && opts.store_kind != 2;
+  if (bulk) {
+    const int h_row = epi.hstride > 0 ? epi.hstride : shp.H;
+    for (int j = 0; j < epi.P; ++j) {
+      const int c = epi.cbase + (j < epi.crem ? 1 : 0);
+      if (c == 0) continue;
+      if (!make_out_map(&maps.o[j], epi.part[j], shp.B, shp.H, h_row, c, shp.d)) return ATTN_A2A_ECUDA;
+    }
+  }
   if (!make_map(&maps.q[0], q, shp.B, shp.H, shp.S, shp.d, shp.q_sb, shp.q_sh, shp.q_ss) ||
       !make_map(&maps.k[0], k, shp.B, shp.H, shp.S, shp.d, shp.k_sb, shp.k_sh, shp.k_ss) ||
       !make_map(&maps.v[0], v, shp.B, shp.H, shp.S, shp.d, shp.v_sb, shp.v_sh, shp.v_ss))
@@ -107,6 +141,9 @@ int launch_fa_tc(const void* q, const void* k, const void* v, const attn_a2a_sha
     p.interleave = epi.cbase / (2 * tc::kBM);
   const int grid = grid_for(p, opts);
   if (grid <= 0) return ATTN_A2A_ECUDA;
+  if (bulk)
+    return shp.d == 128 ? launch_t<128, tc::kModeA2AT, 1>(maps, p, grid, stream)
+                        : launch_t<64, tc::kModeA2AT, 1>(maps, p, grid, stream);
   if (shp.d == 128)
     return a2a ? launch_t<128, tc::kModeA2A, 1>(maps, p, grid, stream)
                : launch_t<128, tc::kModeContig, 1>(maps, p, grid, stream);

@@ -94,12 +94,21 @@ struct Cfg {
   static constexpr int QF = 0, QE = 2, SF = 4, PF = 6, OF = 8, OE = 10, KVF = 12;
   static constexpr int KVE = KVF + NSTAGE;
   static constexpr int DONE = KVE + NSTAGE;
-  static constexpr int NBAR = DONE + 1;
+  // bulk-store epilogue: STG = the staging buffer is free again (one phase per
+  // tile epilogue, in the order tile 0, tile 1, tile 0, ...); STGW + t = the
+  // four warps of tile t have written their rows
+  static constexpr int STG = DONE + 1, STGW = DONE + 2;
+  static constexpr int NBAR = STGW + 2;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   // MISC: +0 abort flag, +4 TMEM base, +8 relay event count
   static constexpr int CNT_EV = MISC_OFF + 8;
   static constexpr int SMEM_USED = MISC_OFF + 16;
   static constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack for 1024-byte alignment
+  // the bulk-store epilogue's staging buffer: one 128-row output tile in
+  // 128-byte-swizzled 64-column atoms, shared by the two query tiles in turn
+  static constexpr int STG_OFF = (SMEM_USED + 1023) / 1024 * 1024;
+  static constexpr int SMEM_ALLOC_STG = STG_OFF + TILE_BYTES + 1024;
+  static_assert(SMEM_ALLOC_STG <= 227 * 1024, "staging buffer does not fit");
 };
 
 // Where the output tile goes and where the inputs come from:
@@ -111,12 +120,19 @@ struct Cfg {
 //                Query tiles and key blocks are then counted per partition,
 //                starting at each partition's row 0, so that none straddles two
 //                partitions; only a partition's last block can be partial.
-enum : int { kModeContig = 0, kModeA2A = 1, kModeS2S = 2 };
+//   kModeA2AT    as kModeA2A, but each output tile goes out as bulk tensor
+//                stores (TMA) from a shared-memory staging buffer: the owner
+//                commits the bulk group and resumes; only the buffer's reuse
+//                waits, for the stores' shared-memory reads. A tile that
+//                straddles two partitions is stored row by row as in kModeA2A.
+enum : int { kModeContig = 0, kModeA2A = 1, kModeS2S = 2, kModeA2AT = 3 };
 constexpr int kMaxS2SRanks = 8;
+constexpr int kMaxStoreMaps = 8;  // output partitions with a tensor map (bulk-store epilogue)
 
 template <int N>
 struct Maps {
   CUtensorMap q[N], k[N], v[N];
+  CUtensorMap o[kMaxStoreMaps];  // output partitions, bulk-store epilogue only
 };
 
 struct Params {
@@ -473,8 +489,45 @@ __device__ __forceinline__ float probs(const uint32_t (&sr)[128], uint32_t (&pk)
   return s0 + s1;
 }
 
-template <int D, int MODE>
-__device__ void softmax_role(const Params& p, int t, uint32_t bar0, uint32_t tmem, const WaitCtl& w) {
+// Bulk-store epilogue of one tile (kModeA2AT): the 128 owner threads write
+// their normalised bf16 rows into the staging buffer (128-byte swizzle, as
+// the tensor map expects), hand them to the async proxy, and one elected
+// thread issues the tile's tensor stores into partition j0 from local row l0,
+// commits the bulk group, waits only until the buffer has been read, and
+// passes the buffer on. Returns false on abort.
+template <int D, int NMAP>
+__device__ __forceinline__ bool bulk_store_tile(const Maps<NMAP>* maps, uint32_t stg, uint32_t bar_stg,
+                                                uint32_t bar_stgw, uint32_t stg_parity, uint32_t stgw_parity,
+                                                bool wait_stg, int r, int lane, bool elected, const uint32_t (&o)[D],
+                                                float inv_l, int j0, int l0, int h, int b, const WaitCtl& w) {
+  if (wait_stg && !__all_sync(0xffffffffu, mbar_wait(bar_stg, stg_parity, w))) return false;
+#pragma unroll
+  for (int c = 0; c < D / 8; ++c) {
+    const uint32_t a = static_cast<uint32_t>(c / 8) * (128u * 128u);  // 64-column atom
+    const uint32_t addr = stg + a + static_cast<uint32_t>(r) * 128u + static_cast<uint32_t>(((c % 8) ^ (r & 7)) * 16);
+    const uint32_t x = pack_bf16x2(__uint_as_float(o[8 * c + 0]) * inv_l, __uint_as_float(o[8 * c + 1]) * inv_l);
+    const uint32_t y = pack_bf16x2(__uint_as_float(o[8 * c + 2]) * inv_l, __uint_as_float(o[8 * c + 3]) * inv_l);
+    const uint32_t z = pack_bf16x2(__uint_as_float(o[8 * c + 4]) * inv_l, __uint_as_float(o[8 * c + 5]) * inv_l);
+    const uint32_t v = pack_bf16x2(__uint_as_float(o[8 * c + 6]) * inv_l, __uint_as_float(o[8 * c + 7]) * inv_l);
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(x), "r"(y), "r"(z), "r"(v) : "memory");
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar_stgw);
+  if (elected) {
+    if (!mbar_wait(bar_stgw, stgw_parity, w)) return false;
+#pragma unroll
+    for (int a = 0; a < D / 64; ++a) tma_store_4d(&maps->o[j0], stg + a * 128 * 128, a * 64, h, l0, b);
+    bulk_commit_group();
+    bulk_wait_read_all();  // the buffer may be reused once the stores have read it
+    mbar_arrive(bar_stg);
+  }
+  return true;
+}
+
+template <int D, int MODE, int NMAP>
+__device__ void softmax_role(const Params& p, int t, uint32_t bar0, uint32_t tmem, const Maps<NMAP>* maps,
+                             uint32_t stg, const WaitCtl& w) {
   using C = Cfg<D>;
   auto BAR = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -484,6 +537,7 @@ __device__ void softmax_role(const Params& p, int t, uint32_t bar0, uint32_t tme
   const uint32_t tO = tmem + lane_off + 256 + t * D;
   const float sl2 = p.scale_log2;
   uint32_t sf_cnt = 0;
+  uint32_t stgw_cnt = 0;  // this tile's bulk stores so far (phases of STGW + t)
   int it = 0;
   for (int item = blockIdx.x; item < p.total; item += gridDim.x, ++it) {
     const Item wi = decode_item(p, item);
@@ -553,6 +607,30 @@ __device__ void softmax_role(const Params& p, int t, uint32_t bar0, uint32_t tme
     else tmem_ld_x64(tO, o);
     tc_fence_before();
     mbar_arrive(BAR(C::OE + t));  // O_t may now be overwritten by the next item
+    if constexpr (MODE == kModeA2AT) {
+      // Epilogue uses are numbered u = 2 it + t; use u waits until use u - 1
+      // has released the staging buffer (token STG, one phase per use).
+      const uint32_t u = 2u * static_cast<uint32_t>(it) + static_cast<uint32_t>(t);
+      const bool elected = (warp & 3) == 0 && lane == 0;
+      const int s0 = (2 * wi.pair + t) * kBM;  // the tile's first sequence row
+      int j0 = 0, l0 = 0, c0 = 0, j1 = -1, l1, c1;
+      if (s0 < p.S) {
+        chunk_of_row(p.epi, s0, j0, l0, c0);
+        chunk_of_row(p.epi, min(s0 + kBM, p.S) - 1, j1, l1, c1);
+      }
+      if (s0 < p.S && j0 == j1 && j0 < kMaxStoreMaps) {  // the whole tile lands in one partition
+        if (!bulk_store_tile<D, NMAP>(maps, stg, BAR(C::STG), BAR(C::STGW + t), (u - 1) & 1u, stgw_cnt & 1u,
+                                      u > 0, r, lane, elected, o, 1.0f / l, j0, l0, wi.h, wi.b, w))
+          return;
+        ++stgw_cnt;
+        continue;
+      }
+      // no bulk store for this tile: pass the buffer on in turn
+      if (elected) {
+        if (u > 0 && !mbar_wait(BAR(C::STG), (u - 1) & 1u, w)) return;
+        mbar_arrive(BAR(C::STG));
+      }
+    }
     uint16_t* dst = nullptr;
     if constexpr (MODE == kModeS2S) {
       const int qt = 2 * wi.pair + t;
@@ -564,7 +642,7 @@ __device__ void softmax_role(const Params& p, int t, uint32_t bar0, uint32_t tme
                 ((static_cast<int64_t>(wi.b) * bq.c + lrow) * p.H + wi.h) * D;
       }
     } else if (srow < p.S) {
-      dst = out_row_ptr<D, MODE == kModeA2A>(p.epi, p.B, p.H, p.S, wi.b, wi.h, srow);
+      dst = out_row_ptr<D, MODE == kModeA2A || MODE == kModeA2AT>(p.epi, p.B, p.H, p.S, wi.b, wi.h, srow);
     }
     if (dst != nullptr) {
       const float inv_l = 1.0f / l;
@@ -611,12 +689,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(BAR(C::KVE + s), 1);
     }
     mbar_init(BAR(C::DONE), 1);
+    mbar_init(BAR(C::STG), 1);
+    mbar_init(BAR(C::STGW + 0), 4);  // one arrive per warp of the tile
+    mbar_init(BAR(C::STGW + 1), 4);
     *abort_flag = 0;
     reinterpret_cast<uint32_t*>(sgen + C::MISC_OFF)[2] = 0;  // relay event count
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
     const int nmaps = MODE == kModeS2S ? p.epi.P : 1;
+    if (MODE == kModeA2AT)
+      for (int i = 0; i < p.epi.P && i < kMaxStoreMaps; ++i)
+        if (p.epi.cbase > 0 || i < p.epi.crem) tma_prefetch_desc(&maps.o[i]);  // partitions with rows only
     for (int i = 0; i < nmaps; ++i) {
       tma_prefetch_desc(&maps.q[i]);
       tma_prefetch_desc(&maps.k[i]);
@@ -644,7 +728,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
-    softmax_role<D, MODE>(p, (warp - 4) / 4, bar0, tmem, w);
+    softmax_role<D, MODE, NMAP>(p, (warp - 4) / 4, bar0, tmem, &maps, sbase + C::STG_OFF, w);
+    // the bulk-store issuers: every store must have completed before the CTA exits
+    if (MODE == kModeA2AT && (warp & 3) == 0 && lane == 0) bulk_wait_all();
   }
   tc_fence_before();
   __syncthreads();

@@ -6,9 +6,10 @@ S grows, contradicting a completion-coupled model whose overhead grows with
 S; "Key Contributions": neither fully blocking nor unbounded-asynchronous
 models capture issuer-visible behaviour).
 
-For each S the same kernel runs with the all-to-all epilogue (fused) and with
-the contiguous epilogue (attention alone); the serial baseline adds the
-separate permute. The models, per work item of a CTA (two 128-row tiles, so
+For each S the same kernel runs with the all-to-all epilogue (fused; with its
+default bulk tensor stores and with row stores from registers) and with the
+contiguous epilogue (attention alone); the serial baseline adds the separate
+permute. The models, per work item of a CTA (two 128-row tiles, so
 V_item = 2 * 128 * 2d bytes of stores, and a compute gap G_item = the item's
 share of attention-alone time):
 
@@ -87,7 +88,8 @@ def report(H=40, d=128, P=8):
         parts = bd.alloc_partitions(1, S, H, d, P)
         o = torch.empty((1, H, S, d), dtype=torch.bfloat16, device="cuda")
         n = max(5, int(2e11 / cfg.flops * 50)) if cfg.flops < 2e11 else 10
-        t_f = time_ms(lambda: bd.attn_a2a_fwd(q, k, v, P, cfg.scale, parts), n)
+        t_f = time_ms(lambda: bd.attn_a2a_fwd(q, k, v, P, cfg.scale, parts), n)  # bulk tensor stores
+        t_r = time_ms(lambda: bd.attn_a2a_fwd(q, k, v, P, cfg.scale, parts, store_kind=2), n)  # row stores
         t_c = time_ms(lambda: bd.attn_a2a_fwd_contig(q, k, v, cfg.scale, o), n)
         t_p = time_ms(lambda: bd.attn_a2a_permute(o, P, parts), n)
         items = H * ((S + 127) // 128 + 1) // 2
@@ -98,8 +100,9 @@ def report(H=40, d=128, P=8):
         t0 = t0_of(table, V)
         burst_gap = bg.predict_t_iss(g_item, t0, V, R) * items_per_sm
         coupled = (t0 + V / R) * items_per_sm
-        rows.append({"S": S, "fused_ms": t_f, "contig_ms": t_c, "permute_ms": t_p,
-                     "measured_overhead": t_f / t_c - 1, "serial_over_fused": (t_c + t_p) / t_f,
+        rows.append({"S": S, "fused_ms": t_f, "fused_row_stores_ms": t_r, "contig_ms": t_c, "permute_ms": t_p,
+                     "measured_overhead": t_f / t_c - 1, "measured_overhead_row_stores": t_r / t_c - 1,
+                     "serial_over_fused": (t_c + t_p) / t_f,
                      "pred_burst_gap": burst_gap / (t_c * 1e-3),
                      "pred_completion_coupled": coupled / (t_c * 1e-3),
                      "pred_unbounded_async": 0.0, "items_per_sm": items_per_sm,

@@ -434,7 +434,7 @@ def main():
         "pct_of_bf16_peak_sustained": 100.0 * tflops / peaks.get("bf16_tflops_sustained", peak),
         "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
                      "frac": tflops / peak, "traffic": traffic,
-                     "kernel": "fa_fwd_tc_kernel<128, a2a>", "peak_source": f"{peak_src} bf16_tflops (burst)"},
+                     "kernel": "fa_fwd_tc_kernel<128, a2a, bulk-store epilogue>", "peak_source": f"{peak_src} bf16_tflops (burst)"},
         "attention_alone_ms": ms_contig,
         "permute_ms": ms_permute,
         "serial_ms": ms_serial,

@@ -73,9 +73,18 @@ typedef struct {
 /* Tuning and test options for the *_ex entry points. Zero-initialised means
  * the defaults used by the plain entry points. */
 typedef struct {
-  int store_kind;       /* 0: vector st.global of each owned output row straight from
-                           registers (the only epilogue built; any other value returns
-                           ATTN_A2A_EUNSUPPORTED) */
+  int store_kind;       /* how the tile owner stores its output tile:
+                           0 = automatic: 1 where it is built (the all-to-all layout
+                               with P <= 8), else 2;
+                           1 = bulk tensor stores (TMA) from a shared-memory staging
+                               tile: the owner commits the bulk group and resumes,
+                               waiting only until the stores have read the staging
+                               tile before reusing it; a tile that straddles two
+                               partitions is stored as in 2. All-to-all layout with
+                               P <= 8 only, else ATTN_A2A_EUNSUPPORTED;
+                           2 = vector st.global of each owned output row straight
+                               from registers.
+                           Results are identical; values > 2 are ATTN_A2A_EINVAL */
   int grid;             /* persistent CTAs; 0 = one per SM */
   long long timeout_ns; /* limit of every in-kernel wait; 0 = 2 000 000 000 ns */
   int inject_stall;     /* test hook, 0 in normal use. 1 = the softmax role of the first

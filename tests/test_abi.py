@@ -88,7 +88,9 @@ def test_fwd_rejects_bad_arguments(lib, kw, code):
 
 def test_bad_options_rejected(lib):
     assert call_fwd(lib, opts=bd._opts(store_kind=7)) == bd.EINVAL
-    assert call_fwd(lib, opts=bd._opts(store_kind=1)) == bd.EUNSUPPORTED
+    assert call_fwd(lib, opts=bd._opts(store_kind=3)) == bd.EINVAL
+    # the bulk-store epilogue exists for the all-to-all layout with at most 8 partitions
+    assert call_fwd(lib, P=16, H=16, opts=bd._opts(store_kind=1)) == bd.EUNSUPPORTED
     assert call_fwd(lib, opts=bd._opts(grid=-1)) == bd.EINVAL
     assert call_fwd(lib, opts=bd._opts(timeout_ns=-5)) == bd.EINVAL
     assert call_fwd(lib, opts=bd._opts(tile_order=2)) == bd.EINVAL
@@ -102,6 +104,9 @@ def test_empty_problem_is_ok_without_launch(lib):
 
 def test_contig_and_permute_validation(lib):
     shp = bd.plain_shape(1, 4, 256, 64)
+    # no bulk-store epilogue for the contiguous layout
+    assert lib.attn_a2a_fwd_contig_ex(FAKE, FAKE * 2, FAKE * 3, ctypes.byref(shp), 0.1, FAKE * 16, None,
+                                      ctypes.byref(bd._opts(store_kind=1)), None) == bd.EUNSUPPORTED
     assert lib.attn_a2a_fwd_contig(FAKE, FAKE * 2, FAKE * 3, ctypes.byref(shp), 0.1, None, None, None) == bd.EINVAL
     # output overlapping q
     assert lib.attn_a2a_fwd_contig(FAKE, FAKE * 4, FAKE * 8, ctypes.byref(shp), 0.1, FAKE + 64, None, None) == bd.EINVAL

@@ -209,3 +209,43 @@ def test_growing_and_jumping_scores_take_the_rescale_path():
     want = orc.head_to_seq_partitions(orc.attention_fp64(q, k, v, scale), P)
     for j, (got, w) in enumerate(zip(g.parts, want)):
         compare(orc.as_f64(got), w, f"growing scores, partition {j}")
+
+
+# The bulk-store epilogue (store_kind = 1, the default where it is built)
+# against the register-store one (store_kind = 2): same arithmetic, so the
+# partitions must match byte for byte. The cases
+# include tiles that straddle two partitions (stored row by row), ragged
+# ends (rows past S are clipped by the tensor store), batch 2, d = 64 and
+# fewer rows than ranks.
+BULK_CASES = [
+    ("tiny", 1, 4, 256, 64, 2),
+    ("image", 1, 24, 4096, 128, 4),
+    ("joint", 1, 24, 4608, 128, 8),
+    ("ragged_1000_P8_d64", 1, 8, 1000, 64, 8),
+    ("ragged_300_P3", 1, 3, 300, 128, 3),
+    ("batch2_odd_blocks", 2, 2, 640, 128, 2),
+    ("S_lt_P", 1, 8, 5, 64, 8),
+]
+
+
+@pytest.mark.parametrize("case", BULK_CASES, ids=[c[0] for c in BULK_CASES])
+def test_bulk_store_epilogue_matches_register_stores(case):
+    cfg = case_cfg(*case)
+    _, _, _, dq, dk, dv = cuda_qkv(cfg, seed=7)
+    a = fused(dq, dk, dv, cfg.P, cfg.scale, store_kind=2)
+    b = fused(dq, dk, dv, cfg.P, cfg.scale, store_kind=1)
+    c = fused(dq, dk, dv, cfg.P, cfg.scale)  # automatic: bulk here
+    assert b.guards_intact() and c.guards_intact(), "bulk stores wrote outside a partition"
+    for x, y, z in zip(a.parts, b.parts, c.parts):
+        assert torch.equal(x.view(torch.int16), y.view(torch.int16))
+        assert torch.equal(y.view(torch.int16), z.view(torch.int16))
+
+
+def test_bulk_store_epilogue_with_interleaved_order():
+    cfg = workloads.CONFIGS["image"]
+    _, _, _, dq, dk, dv = cuda_qkv(cfg, seed=9)
+    a = fused(dq, dk, dv, cfg.P, cfg.scale, store_kind=2)
+    b = fused(dq, dk, dv, cfg.P, cfg.scale, store_kind=1, tile_order=1)
+    assert b.guards_intact()
+    for x, y in zip(a.parts, b.parts):
+        assert torch.equal(x.view(torch.int16), y.view(torch.int16))

@@ -144,8 +144,9 @@ int fwd_common(const void* q, const void* k, const void* v, const attn_a2a_shape
                           opts->timeout_ns < 0 || opts->inject_stall < 0 || opts->inject_stall > 1 ||
                           opts->tile_order < 0 || opts->tile_order > 1))
     return ATTN_A2A_EINVAL;
-  // the bulk-store epilogue exists for the all-to-all layout with up to 8 partitions
-  if (opts != nullptr && opts->store_kind == 1 && (!a2a || P > 8)) return ATTN_A2A_EUNSUPPORTED;
+  // the bulk-store epilogue exists for the contiguous layout and for the
+  // all-to-all layout with up to 8 partitions
+  if (opts != nullptr && opts->store_kind == 1 && a2a && P > 8) return ATTN_A2A_EUNSUPPORTED;
   EpiParams epi;
   std::memset(&epi, 0, sizeof(epi));
   if (a2a) {

@@ -74,7 +74,7 @@ bool make_out_map(CUtensorMap* m, void* base, int B, int H, int H_row, int c, in
 template <int D, int MODE, int NMAP>
 int launch_t(const tc::Maps<NMAP>& maps, const tc::Params& p, int grid, cudaStream_t stream) {
   auto kern = tc::fa_fwd_tc_kernel<D, MODE, NMAP>;
-  constexpr int smem = MODE == tc::kModeA2AT ? tc::Cfg<D>::SMEM_ALLOC_STG : tc::Cfg<D>::SMEM_ALLOC;
+  constexpr int smem = tc::kBulkStores<MODE> ? tc::Cfg<D>::SMEM_ALLOC_STG : tc::Cfg<D>::SMEM_ALLOC;
   // The in-kernel register split assumes exactly this launch register count;
   // with fewer registers at launch the softmax warpgroups could never obtain
   // their share, so refuse to launch rather than risk a stuck kernel.
@@ -112,19 +112,23 @@ int launch_fa_tc(const void* q, const void* k, const void* v, const attn_a2a_sha
                  const attn_a2a_opts& opts, cudaStream_t stream) {
   tc::Maps<1> maps;
   std::memset(&maps, 0, sizeof(maps));
-  // store_kind 0: bulk tensor stores where they are built (the all-to-all
-  // layout with up to kMaxStoreMaps partitions), else row stores; 1: bulk
-  // stores or EUNSUPPORTED; 2: row stores from registers
-  const bool bulk_ok = a2a && epi.P <= tc::kMaxStoreMaps;
+  // store_kind 0: bulk tensor stores where they are built (the contiguous
+  // layout, and the all-to-all layout with up to kMaxStoreMaps partitions),
+  // else row stores; 1: bulk stores or EUNSUPPORTED; 2: row stores
+  const bool bulk_ok = !a2a || epi.P <= tc::kMaxStoreMaps;
   if (opts.store_kind == 1 && !bulk_ok) return ATTN_A2A_EUNSUPPORTED;
   const bool bulk = bulk_ok && opts.store_kind != 2;
-  if (bulk) {
+  if (bulk && a2a) {
     const int h_row = epi.hstride > 0 ? epi.hstride : shp.H;
     for (int j = 0; j < epi.P; ++j) {
       const int c = epi.cbase + (j < epi.crem ? 1 : 0);
       if (c == 0) continue;
       if (!make_out_map(&maps.o[j], epi.part[j], shp.B, shp.H, h_row, c, shp.d)) return ATTN_A2A_ECUDA;
     }
+  }
+  if (bulk && !a2a) {  // [B, H, S, d] contiguous, addressed like the inputs
+    const long long ss = shp.d, sh = ss * shp.S, sb = sh * shp.H;
+    if (!make_map(&maps.o[0], epi.out, shp.B, shp.H, shp.S, shp.d, sb, sh, ss)) return ATTN_A2A_ECUDA;
   }
   if (!make_map(&maps.q[0], q, shp.B, shp.H, shp.S, shp.d, shp.q_sb, shp.q_sh, shp.q_ss) ||
       !make_map(&maps.k[0], k, shp.B, shp.H, shp.S, shp.d, shp.k_sb, shp.k_sh, shp.k_ss) ||
@@ -141,9 +145,12 @@ int launch_fa_tc(const void* q, const void* k, const void* v, const attn_a2a_sha
     p.interleave = epi.cbase / (2 * tc::kBM);
   const int grid = grid_for(p, opts);
   if (grid <= 0) return ATTN_A2A_ECUDA;
-  if (bulk)
+  if (bulk && a2a)
     return shp.d == 128 ? launch_t<128, tc::kModeA2AT, 1>(maps, p, grid, stream)
                         : launch_t<64, tc::kModeA2AT, 1>(maps, p, grid, stream);
+  if (bulk)
+    return shp.d == 128 ? launch_t<128, tc::kModeContigT, 1>(maps, p, grid, stream)
+                        : launch_t<64, tc::kModeContigT, 1>(maps, p, grid, stream);
   if (shp.d == 128)
     return a2a ? launch_t<128, tc::kModeA2A, 1>(maps, p, grid, stream)
                : launch_t<128, tc::kModeContig, 1>(maps, p, grid, stream);

@@ -74,14 +74,15 @@ typedef struct {
  * the defaults used by the plain entry points. */
 typedef struct {
   int store_kind;       /* how the tile owner stores its output tile:
-                           0 = automatic: 1 where it is built (the all-to-all layout
-                               with P <= 8), else 2;
+                           0 = automatic: 1 where it is built (the contiguous
+                               layout, and the all-to-all layout with P <= 8),
+                               else 2;
                            1 = bulk tensor stores (TMA) from a shared-memory staging
                                tile: the owner commits the bulk group and resumes,
                                waiting only until the stores have read the staging
                                tile before reusing it; a tile that straddles two
-                               partitions is stored as in 2. All-to-all layout with
-                               P <= 8 only, else ATTN_A2A_EUNSUPPORTED;
+                               partitions is stored as in 2. All-to-all layout
+                               with P > 8: ATTN_A2A_EUNSUPPORTED;
                            2 = vector st.global of each owned output row straight
                                from registers.
                            Results are identical; values > 2 are ATTN_A2A_EINVAL */

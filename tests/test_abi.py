@@ -104,9 +104,8 @@ def test_empty_problem_is_ok_without_launch(lib):
 
 def test_contig_and_permute_validation(lib):
     shp = bd.plain_shape(1, 4, 256, 64)
-    # no bulk-store epilogue for the contiguous layout
     assert lib.attn_a2a_fwd_contig_ex(FAKE, FAKE * 2, FAKE * 3, ctypes.byref(shp), 0.1, FAKE * 16, None,
-                                      ctypes.byref(bd._opts(store_kind=1)), None) == bd.EUNSUPPORTED
+                                      ctypes.byref(bd._opts(store_kind=3)), None) == bd.EINVAL
     assert lib.attn_a2a_fwd_contig(FAKE, FAKE * 2, FAKE * 3, ctypes.byref(shp), 0.1, None, None, None) == bd.EINVAL
     # output overlapping q
     assert lib.attn_a2a_fwd_contig(FAKE, FAKE * 4, FAKE * 8, ctypes.byref(shp), 0.1, FAKE + 64, None, None) == bd.EINVAL

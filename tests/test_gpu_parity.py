@@ -249,3 +249,22 @@ def test_bulk_store_epilogue_with_interleaved_order():
     assert b.guards_intact()
     for x, y in zip(a.parts, b.parts):
         assert torch.equal(x.view(torch.int16), y.view(torch.int16))
+
+
+@pytest.mark.parametrize("B,H,S,d", [(1, 4, 1000, 128), (2, 3, 333, 64), (1, 2, 129, 128)])
+def test_contiguous_bulk_store_epilogue_matches_row_stores(B, H, S, d):
+    # attention alone: bulk tensor stores of [B, H, S, d] (the default) against
+    # row stores; rows past S are clipped by the tensor store
+    cfg = workloads.AttnConfig("contig", B=B, H=H, S=S, d=d, P=1)
+    _, _, _, dq, dk, dv = cuda_qkv(cfg, seed=10)
+    pad = 512
+    outs = []
+    for kind in (2, 1, 0):
+        buf = torch.full((B * H * S * d + 2 * pad,), -12345.0, dtype=torch.bfloat16, device="cuda")
+        o = buf[pad:pad + B * H * S * d].view(B, H, S, d)
+        bd.attn_a2a_fwd_contig(dq, dk, dv, cfg.scale, o, store_kind=kind)
+        torch.cuda.synchronize()
+        assert torch.all(buf[:pad] == -12345.0) and torch.all(buf[-pad:] == -12345.0)
+        outs.append(o.clone())
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    assert torch.equal(outs[0].view(torch.int16), outs[2].view(torch.int16))

@@ -101,8 +101,14 @@ def time_orders(E=32, T=512, K=1024, N=512, P=8, experts_per_wave=None, reps=20)
 def main(argv=None) -> int:
     ap = argparse.ArgumentParser()
     ap.add_argument("--out", default=None)
+    ap.add_argument("--shape", default=None, help="E,T,K,N: time this one problem instead of the K sweep")
+    ap.add_argument("--reps", type=int, default=20)
     a = ap.parse_args(argv)
-    rows = [time_orders(K=K) for K in (128, 256, 512, 1024, 2048)]
+    if a.shape:
+        E, T, K, N = (int(v) for v in a.shape.split(","))
+        rows = [time_orders(E=E, T=T, K=K, N=N, reps=a.reps)]
+    else:
+        rows = [time_orders(K=K, reps=a.reps) for K in (128, 256, 512, 1024, 2048)]
     text = json.dumps(rows, indent=1)
     if a.out:
         with open(a.out, "w") as fh:

@@ -37,6 +37,14 @@ METRIC = "fused attn+A2A-layout TFLOP/s and % of bf16 dense tensor peak, 1 GB300
 WORKLOAD = "video DiT attention + Ulysses post-attention A2A layout: B=1, H=40, S=32768, d=128, P=8 virtual ranks"
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 KERNEL_SOURCES = ["fa_tc.cuh", "ptx.cuh", "epilogue.cuh", "tmem_ops.cuh", "fa_tc.cu"]
+BULK_A2A_MAX_BLOCKS = 128  # the library's automatic store kind: bulk tensor stores up to S = 16384
+
+
+def fused_kernel_label(cfg) -> str:
+    """The kernel instantiation the fused call launches for cfg (the ncu name)."""
+    bulk = cfg.P <= 8 and -(-cfg.S // 128) <= BULK_A2A_MAX_BLOCKS
+    return (f"fa_fwd_tc_kernel<{cfg.d}, {3 if bulk else 1}, 1> (all-to-all layout, "
+            f"{'bulk-store' if bulk else 'row-store'} epilogue)")
 
 
 def dist_env():
@@ -434,7 +442,7 @@ def main():
         "pct_of_bf16_peak_sustained": 100.0 * tflops / peaks.get("bf16_tflops_sustained", peak),
         "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
                      "frac": tflops / peak, "traffic": traffic,
-                     "kernel": "fa_fwd_tc_kernel<128, a2a, bulk-store epilogue>", "peak_source": f"{peak_src} bf16_tflops (burst)"},
+                     "kernel": fused_kernel_label(cfg), "peak_source": f"{peak_src} bf16_tflops (burst)"},
         "attention_alone_ms": ms_contig,
         "permute_ms": ms_permute,
         "serial_ms": ms_serial,

@@ -74,9 +74,9 @@ typedef struct {
  * the defaults used by the plain entry points. */
 typedef struct {
   int store_kind;       /* how the tile owner stores its output tile:
-                           0 = automatic: 1 where it is built (the contiguous
-                               layout, and the all-to-all layout with P <= 8),
-                               else 2;
+                           0 = automatic: 1 for the contiguous layout and for the
+                               all-to-all layout with P <= 8 and S <= 16384 (where
+                               it measured faster), else 2;
                            1 = bulk tensor stores (TMA) from a shared-memory staging
                                tile: the owner commits the bulk group and resumes,
                                waiting only until the stores have read the staging

@@ -241,6 +241,20 @@ def test_bulk_store_epilogue_matches_register_stores(case):
         assert torch.equal(y.view(torch.int16), z.view(torch.int16))
 
 
+@pytest.mark.parametrize("S", [16384, 16385, 20000])
+def test_automatic_store_kind_around_its_switch(S):
+    # the automatic kind takes bulk stores up to 128 key blocks (S = 16384)
+    # and row stores above; every kind writes the same bytes
+    cfg = workloads.AttnConfig(f"switch_{S}", B=1, H=2, S=S, d=128, P=2)
+    _, _, _, dq, dk, dv = cuda_qkv(cfg, seed=14)
+    outs = [fused(dq, dk, dv, cfg.P, cfg.scale, store_kind=kind) for kind in (0, 1, 2)]
+    for g in outs:
+        assert g.guards_intact()
+    for x, y, z in zip(*(g.parts for g in outs)):
+        assert torch.equal(x.view(torch.int16), y.view(torch.int16))
+        assert torch.equal(x.view(torch.int16), z.view(torch.int16))
+
+
 def test_bulk_store_epilogue_with_interleaved_order():
     cfg = workloads.CONFIGS["image"]
     _, _, _, dq, dk, dv = cuda_qkv(cfg, seed=9)

@@ -35,6 +35,7 @@ EXPORTED = (
     "moe_gemm_scatter",
     "attn_a2a_strerror",
     "attn_a2a_num_sms",
+    "attn_a2a_store_kind",
 )
 
 
@@ -110,6 +111,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.attn_a2a_strerror.argtypes = [cint]
     lib.attn_a2a_strerror.restype = ctypes.c_char_p
     lib.attn_a2a_num_sms.argtypes = []
+    lib.attn_a2a_store_kind.argtypes = [cint, cint, cint, cint, ctypes.POINTER(ctypes.c_int)]
     for name in EXPORTED:
         if name != "attn_a2a_strerror":
             getattr(lib, name).restype = cint
@@ -308,3 +310,12 @@ def attn_a2a_strerror(code: int) -> str:
 
 def attn_a2a_num_sms() -> int:
     return num_sms()
+
+
+def attn_a2a_store_kind(S: int, P: int, layout: int, store_kind: int = 0) -> int:
+    """Store kind the library uses for these sizes: 1 = bulk tensor stores, 2 = row stores.
+    layout 0 = contiguous (attention alone), 1 = all-to-all. Raises AttnA2AError on a bad request."""
+    out = ctypes.c_int(0)
+    rc = load().attn_a2a_store_kind(int(S), int(P), int(layout), int(store_kind), ctypes.byref(out))
+    _check(rc, "attn_a2a_store_kind", True)
+    return out.value

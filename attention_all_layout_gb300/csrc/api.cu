@@ -196,6 +196,16 @@ const char* attn_a2a_strerror(int status) {
 
 int attn_a2a_num_sms(void) { return num_sms_current_device(); }
 
+int attn_a2a_store_kind(int S, int P, int layout, int store_kind, int* resolved) {
+  if (resolved == nullptr || S < 0 || P < 1 || P > kMaxRanks || layout < 0 || layout > 1 || store_kind < 0 ||
+      store_kind > 2)
+    return ATTN_A2A_EINVAL;
+  const int kind = resolve_store_kind(S, P, layout == 1, store_kind);
+  if (kind == 0) return ATTN_A2A_EUNSUPPORTED;
+  *resolved = kind;
+  return ATTN_A2A_OK;
+}
+
 int attn_a2a_fwd_ex(const void* q, const void* k, const void* v, const attn_a2a_shape* shp, int P,
                     float scale, void* const* out_partitions, int* dev_status,
                     const attn_a2a_opts* opts, void* stream) {

@@ -20,6 +20,23 @@ namespace {
 // 0.997, 16384 0.999, 24576 1.008, 32768 1.004, 75600 1.008.
 constexpr int kBulkA2AMaxBlocks = 128;
 
+}  // namespace
+
+// store_kind 0: bulk tensor stores where they are built and measured faster -
+// the contiguous layout, and the all-to-all layout with up to kMaxStoreMaps
+// partitions and at most kBulkA2AMaxBlocks key blocks (at longer sequences its
+// strided tile stores measured slower than row stores) - else row stores;
+// 1: bulk stores, or 0 where they are not built; 2: row stores.
+int resolve_store_kind(int S, int P, bool a2a, int store_kind) {
+  const bool built = !a2a || P <= tc::kMaxStoreMaps;
+  if (store_kind == 1) return built ? 1 : 0;
+  if (store_kind == 2) return 2;
+  const bool faster = !a2a || (S + tc::kBM - 1) / tc::kBM <= kBulkA2AMaxBlocks;
+  return built && faster ? 1 : 2;
+}
+
+namespace {
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -118,15 +135,9 @@ int launch_fa_tc(const void* q, const void* k, const void* v, const attn_a2a_sha
                  const attn_a2a_opts& opts, cudaStream_t stream) {
   tc::Maps<1> maps;
   std::memset(&maps, 0, sizeof(maps));
-  // store_kind 0: bulk tensor stores where they are built and measured
-  // faster - the contiguous layout, and the all-to-all layout with up to
-  // kMaxStoreMaps partitions and at most kBulkA2AMaxBlocks key blocks (at
-  // longer sequences its strided tile stores measured 0.4-0.9 % slower than
-  // row stores) - else row stores; 1: bulk stores or EUNSUPPORTED; 2: row stores
-  const bool bulk_ok = !a2a || epi.P <= tc::kMaxStoreMaps;
-  if (opts.store_kind == 1 && !bulk_ok) return ATTN_A2A_EUNSUPPORTED;
-  const bool bulk_auto = !a2a || (shp.S + tc::kBM - 1) / tc::kBM <= kBulkA2AMaxBlocks;
-  const bool bulk = bulk_ok && (opts.store_kind == 1 || (opts.store_kind == 0 && bulk_auto));
+  const int kind = resolve_store_kind(shp.S, epi.P, a2a, opts.store_kind);
+  if (kind == 0) return ATTN_A2A_EUNSUPPORTED;
+  const bool bulk = kind == 1;
   if (bulk && a2a) {
     const int h_row = epi.hstride > 0 ? epi.hstride : shp.H;
     for (int j = 0; j < epi.P; ++j) {

@@ -16,6 +16,12 @@ struct Problem {
 
 int num_sms_current_device();
 
+// The epilogue's store kind for a request: 1 = bulk tensor stores, 2 = row
+// stores, or 0 when store_kind 1 asks for bulk stores where they are not
+// built (the all-to-all layout with P > 8). store_kind 0 picks what measured
+// faster; it must be 0, 1 or 2.
+int resolve_store_kind(int S, int P, bool a2a, int store_kind);
+
 int launch_fa_tc(const void* q, const void* k, const void* v, const attn_a2a_shape& shp,
                  float scale, bool a2a, const EpiParams& epi, int* dev_status,
                  const attn_a2a_opts& opts, cudaStream_t stream);

@@ -40,7 +40,6 @@ from . import workloads
 
 S_LIST = (1024, 2048, 4096, 8192, 16384, 32768)
 ROUNDS = 3
-BULK_A2A_MAX_BLOCKS = 128  # the library's automatic store kind: bulk tensor stores up to S = 16384
 
 
 def time_ms(fn, n):
@@ -106,7 +105,7 @@ def report(H=40, d=128, P=8):
                 samples[name].append(time_ms(fn, n))
         med = {name: sorted(v)[len(v) // 2] for name, v in samples.items()}
         t_f, t_r, t_c, t_cr, t_p = med["f"], med["r"], med["c"], med["cr"], med["p"]
-        t_auto = t_f if (S + 127) // 128 <= BULK_A2A_MAX_BLOCKS else t_r  # the automatic store kind
+        t_auto = t_f if bd.attn_a2a_store_kind(S, P, 1) == 1 else t_r  # the automatic store kind
         items = H * ((S + 127) // 128 + 1) // 2
         items_per_sm = -(-items // n_sm)
         g_item = t_c * 1e-3 / items_per_sm

@@ -37,12 +37,13 @@ METRIC = "fused attn+A2A-layout TFLOP/s and % of bf16 dense tensor peak, 1 GB300
 WORKLOAD = "video DiT attention + Ulysses post-attention A2A layout: B=1, H=40, S=32768, d=128, P=8 virtual ranks"
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 KERNEL_SOURCES = ["fa_tc.cuh", "ptx.cuh", "epilogue.cuh", "tmem_ops.cuh", "fa_tc.cu"]
-BULK_A2A_MAX_BLOCKS = 128  # the library's automatic store kind: bulk tensor stores up to S = 16384
 
 
 def fused_kernel_label(cfg) -> str:
     """The kernel instantiation the fused call launches for cfg (the ncu name)."""
-    bulk = cfg.P <= 8 and -(-cfg.S // 128) <= BULK_A2A_MAX_BLOCKS
+    from attention_all_layout_gb300 import binding as bd
+
+    bulk = bd.attn_a2a_store_kind(cfg.S, cfg.P, 1) == 1
     return (f"fa_fwd_tc_kernel<{cfg.d}, {3 if bulk else 1}, 1> (all-to-all layout, "
             f"{'bulk-store' if bulk else 'row-store'} epilogue)")
 

@@ -305,6 +305,16 @@ const char* attn_a2a_strerror(int status);
  * (0 if no device). Host-only query, no launch. */
 int attn_a2a_num_sms(void);
 
+/* The store kind (attn_a2a_opts.store_kind) a call would use for its output
+ * tiles: 1 = bulk tensor stores from a staging tile, 2 = row stores from
+ * registers. S = sequence length, P = partitions (1 for the contiguous
+ * layout), layout = 0 contiguous ("attention alone"), 1 all-to-all;
+ * store_kind = the requested kind, 0 for the automatic choice. Writes the
+ * kind to *resolved (host int) and returns ATTN_A2A_OK;
+ * ATTN_A2A_EUNSUPPORTED where store_kind 1 is not built (all-to-all with
+ * P > 8); ATTN_A2A_EINVAL for arguments out of range. Host-only, no launch. */
+int attn_a2a_store_kind(int S, int P, int layout, int store_kind, int* resolved);
+
 #ifdef __cplusplus
 }
 #endif

@@ -96,6 +96,25 @@ def test_bad_options_rejected(lib):
     assert call_fwd(lib, opts=bd._opts(tile_order=2)) == bd.EINVAL
 
 
+def test_store_kind_query(lib):
+    # the automatic kind: bulk tensor stores for the contiguous layout, and for
+    # the all-to-all layout with P <= 8 up to 128 key blocks (S = 16384)
+    assert bd.attn_a2a_store_kind(32768, 1, 0) == 1
+    assert bd.attn_a2a_store_kind(16384, 8, 1) == 1
+    assert bd.attn_a2a_store_kind(16385, 8, 1) == 2
+    assert bd.attn_a2a_store_kind(75600, 8, 1) == 2
+    assert bd.attn_a2a_store_kind(4096, 16, 1) == 2
+    assert bd.attn_a2a_store_kind(0, 2, 1) == 1
+    # an explicit kind is kept where it is built
+    assert bd.attn_a2a_store_kind(32768, 8, 1, store_kind=1) == 1
+    assert bd.attn_a2a_store_kind(1024, 8, 1, store_kind=2) == 2
+    out = ctypes.c_int(0)
+    assert lib.attn_a2a_store_kind(4096, 16, 1, 1, ctypes.byref(out)) == bd.EUNSUPPORTED
+    for args in ((4096, 8, 2, 0), (4096, 0, 1, 0), (4096, 65, 1, 0), (-1, 8, 1, 0), (4096, 8, 1, 3)):
+        assert lib.attn_a2a_store_kind(*args, ctypes.byref(out)) == bd.EINVAL
+    assert lib.attn_a2a_store_kind(4096, 8, 1, 0, None) == bd.EINVAL
+
+
 def test_empty_problem_is_ok_without_launch(lib):
     # S = 0: every chunk is empty, null partitions are allowed, nothing is launched
     assert call_fwd(lib, S=0, parts=[0, 0]) == bd.OK

@@ -52,10 +52,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // [B, H, S, d] bf16 with element strides (sb, sh, ss), d contiguous; box of
-// 64 x 128 rows with the 128-byte swizzle the MMA descriptors expect.
-// Rows beyond S read as zeros.
+// 64 columns x box_rows rows with the 128-byte swizzle the MMA descriptors
+// expect. Rows beyond S read as zeros.
 bool make_map(CUtensorMap* m, const void* base, int B, int H, int S, int d, long long sb,
-              long long sh, long long ss) {
+              long long sh, long long ss, int box_rows = 128) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
   // A size-1 dimension's stride is never used to address memory; give it a
@@ -67,7 +67,7 @@ bool make_map(CUtensorMap* m, const void* base, int B, int H, int S, int d, long
                         static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(B)};
   cuuint64_t strides[3] = {static_cast<cuuint64_t>(ss) * 2, static_cast<cuuint64_t>(sh) * 2,
                            static_cast<cuuint64_t>(sb) * 2};
-  cuuint32_t box[4] = {64, 128, 1, 1};
+  cuuint32_t box[4] = {64, static_cast<cuuint32_t>(box_rows), 1, 1};
   cuuint32_t estride[4] = {1, 1, 1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
                   estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -184,18 +184,33 @@ int launch_fa_tc_s2s(const void* const* qp, const void* const* kp, const void* c
   if (epi.P > tc::kMaxS2SRanks) return ATTN_A2A_EUNSUPPORTED;
   tc::Maps<tc::kMaxS2SRanks> maps;
   std::memset(&maps, 0, sizeof(maps));
+  // Equal partitions whose length is a multiple of 64 but not of 128 would end
+  // every partition in a half-empty block: count tiles over the whole sequence
+  // and load each as two 64-row halves instead (kModeS2SH).
+  const bool halves = epi.crem == 0 && epi.cbase % tc::kBM != 0 && epi.cbase % (tc::kBM / 2) == 0;
   const long long row = static_cast<long long>(shp.H) * shp.d;  // partition j is [B, c_j, H, d]
   for (int j = 0; j < epi.P; ++j) {
     const int c = epi.cbase + (j < epi.crem ? 1 : 0);
     if (c == 0) continue;
     const long long sb = row * c;
-    if (!make_map(&maps.q[j], qp[j], shp.B, shp.H, c, shp.d, sb, shp.d, row) ||
-        !make_map(&maps.k[j], kp[j], shp.B, shp.H, c, shp.d, sb, shp.d, row) ||
-        !make_map(&maps.v[j], vp[j], shp.B, shp.H, c, shp.d, sb, shp.d, row))
+    const int box = halves ? tc::kBM / 2 : tc::kBM;
+    if (!make_map(&maps.q[j], qp[j], shp.B, shp.H, c, shp.d, sb, shp.d, row, box) ||
+        !make_map(&maps.k[j], kp[j], shp.B, shp.H, c, shp.d, sb, shp.d, row, box) ||
+        !make_map(&maps.v[j], vp[j], shp.B, shp.H, c, shp.d, sb, shp.d, row, box))
       return ATTN_A2A_ECUDA;
   }
   tc::Params p{};
   common_params(p, shp, scale, dev_status, opts);
+  if (halves) {
+    p.nblk = (shp.S + tc::kBM - 1) / tc::kBM;
+    p.npair = (p.nblk + 1) / 2;
+    p.total = shp.B * shp.H * p.npair;
+    p.epi = epi;
+    const int grid = grid_for(p, opts);
+    if (grid <= 0) return ATTN_A2A_ECUDA;
+    if (shp.d == 128) return launch_t<128, tc::kModeS2SH, tc::kMaxS2SRanks>(maps, p, grid, stream);
+    return launch_t<64, tc::kModeS2SH, tc::kMaxS2SRanks>(maps, p, grid, stream);
+  }
   p.nb_big = (epi.cbase + 1 + tc::kBM - 1) / tc::kBM;
   p.nb_small = (epi.cbase + tc::kBM - 1) / tc::kBM;
   p.nblk = epi.crem * p.nb_big + (epi.P - epi.crem) * p.nb_small;

@@ -126,9 +126,15 @@ struct Cfg {
 //                waits, for the stores' shared-memory reads. A tile that
 //                straddles two partitions is stored row by row as in kModeA2A.
 //   kModeContigT as kModeContig, with the bulk-store epilogue.
-// (kModeS2S keeps the row stores: with the staging path its register
-// pressure grew and the whole layer measured ≈ 3 % slower.)
-enum : int { kModeContig = 0, kModeA2A = 1, kModeS2S = 2, kModeA2AT = 3, kModeContigT = 4 };
+//   kModeS2SH    as kModeS2S (sequence-sharded in and out), for partitions of
+//                equal length c that is a multiple of 64 but not of 128: tiles
+//                and key blocks are counted over the whole sequence as in
+//                kModeA2A, and every 128-row tile is loaded as two 64-row halves,
+//                each lying inside one partition, so no block is half empty and
+//                the result equals kModeA2A's bit for bit. Output as kModeA2A.
+// (kModeS2S and kModeS2SH keep the row stores: with the staging path the
+// register pressure grew and the whole layer measured ≈ 3 % slower.)
+enum : int { kModeContig = 0, kModeA2A = 1, kModeS2S = 2, kModeA2AT = 3, kModeContigT = 4, kModeS2SH = 5 };
 template <int MODE>
 constexpr bool kBulkStores = MODE == kModeA2AT || MODE == kModeContigT;
 constexpr int kMaxS2SRanks = 8;
@@ -261,6 +267,24 @@ __device__ void producer_role(const Params& p, const Maps<NMAP>* maps, uint32_t 
   uint32_t q_loads[2] = {0, 0};
   bool ok = true;
   int it = 0;
+  // kModeS2SH: rows [row, row + 128) of the sequence as two 64-row boxes, each
+  // from the partition that holds it (equal partitions of p.epi.cbase rows, a
+  // multiple of 64), into the two halves of every 128-row swizzle atom column
+  // (8 KB apart, so each half starts on a 1 KB swizzle boundary). Rows past S
+  // fall past the last partition's end and read as zeros.
+  auto load_halves = [&](uint32_t dst, const CUtensorMap* tmaps, uint32_t bar, int row, const Item& wi,
+                         uint64_t pol) {
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      const int g = row + hf * (kBM / 2);
+      int j = g / p.epi.cbase;
+      if (j > p.epi.P - 1) j = p.epi.P - 1;
+      const int l = g - j * p.epi.cbase;
+#pragma unroll
+      for (int a = 0; a < D / 64; ++a)
+        tma_load_4d(dst + a * C::ATOM_BYTES + hf * (C::ATOM_BYTES / 2), &tmaps[j], bar, a * 64, l, wi.h, wi.b, pol);
+    }
+  };
   for (int item = blockIdx.x; ok && item < p.total; item += gridDim.x, ++it) {
     const Item wi = decode_item(p, item);
     auto load_q = [&](int t) -> bool {
@@ -270,9 +294,13 @@ __device__ void producer_role(const Params& p, const Maps<NMAP>* maps, uint32_t 
       int qt = 2 * wi.pair + t;  // past the last tile (odd count): rows past S read as zeros,
       if (MODE == kModeS2S && qt >= p.nblk) qt = p.nblk - 1;  // or a real tile whose rows are not stored
       const Blk bq = locate_block<MODE>(p, qt);
+      if constexpr (MODE == kModeS2SH) {
+        load_halves(dst, maps->q, BAR(C::QF + t), bq.row, wi, pol_q);
+      } else {
 #pragma unroll
-      for (int a = 0; a < D / 64; ++a)
-        tma_load_4d(dst + a * C::ATOM_BYTES, &maps->q[bq.map], BAR(C::QF + t), a * 64, bq.row, wi.h, wi.b, pol_q);
+        for (int a = 0; a < D / 64; ++a)
+          tma_load_4d(dst + a * C::ATOM_BYTES, &maps->q[bq.map], BAR(C::QF + t), a * 64, bq.row, wi.h, wi.b, pol_q);
+      }
       ++q_loads[t];
       return true;
     };
@@ -286,9 +314,13 @@ __device__ void producer_role(const Params& p, const Maps<NMAP>* maps, uint32_t 
       if (!mbar_wait(BAR(C::KVE + s), ph ^ 1, w)) return false;
       mbar_arrive_expect_tx(BAR(C::KVF + s), C::TILE_BYTES);
       const uint32_t dst = sbase + C::KV_OFF + s * C::TILE_BYTES;
+      if constexpr (MODE == kModeS2SH) {
+        load_halves(dst, is_v ? maps->v : maps->k, BAR(C::KVF + s), bk.row, wi, pol_kv);
+      } else {
 #pragma unroll
-      for (int a = 0; a < D / 64; ++a)
-        tma_load_4d(dst + a * C::ATOM_BYTES, m, BAR(C::KVF + s), a * 64, bk.row, wi.h, wi.b, pol_kv);
+        for (int a = 0; a < D / 64; ++a)
+          tma_load_4d(dst + a * C::ATOM_BYTES, m, BAR(C::KVF + s), a * 64, bk.row, wi.h, wi.b, pol_kv);
+      }
       ++kv_it;
       return true;
     };
@@ -659,7 +691,7 @@ __device__ void softmax_role(const Params& p, int t, uint32_t bar0, uint32_t tme
                 ((static_cast<int64_t>(wi.b) * bq.c + lrow) * p.H + wi.h) * D;
       }
     } else if (srow < p.S) {
-      dst = out_row_ptr<D, MODE == kModeA2A || MODE == kModeA2AT>(p.epi, p.B, p.H, p.S, wi.b, wi.h, srow);
+      dst = out_row_ptr<D, MODE != kModeContig && MODE != kModeContigT>(p.epi, p.B, p.H, p.S, wi.b, wi.h, srow);
     }
     if (dst != nullptr) {
       const float inv_l = 1.0f / l;
@@ -714,7 +746,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    const int nmaps = MODE == kModeS2S ? p.epi.P : 1;
+    const int nmaps = MODE == kModeS2S || MODE == kModeS2SH ? p.epi.P : 1;
     if (MODE == kModeA2AT)
       for (int i = 0; i < p.epi.P && i < kMaxStoreMaps; ++i)
         if (p.epi.cbase > 0 || i < p.epi.crem) tma_prefetch_desc(&maps.o[i]);  // partitions with rows only

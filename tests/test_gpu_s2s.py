@@ -1,7 +1,8 @@
 """GPU parity of attn_a2a_fwd_s2s: the Ulysses layer with both exchanges
 folded in (sequence-sharded q, k, v partitions in, sequence-sharded output
 out) against the float64 oracle, guard bands intact, and bit-identical to
-attn_a2a_fwd when every chunk is a whole number of 128-row tiles."""
+attn_a2a_fwd when every chunk is a whole number of 128-row tiles, or when the
+chunks are equal multiples of 64 rows (each tile then loaded as two halves)."""
 import numpy as np
 import pytest
 import torch
@@ -30,6 +31,9 @@ CASES = [
     ("ragged_c375", 1, 4, 1500, 128, 4),
     ("ragged_c125_d64", 2, 8, 1000, 64, 8),
     ("S_lt_P", 1, 8, 5, 128, 8),
+    # equal chunks of 64 (mod 128) rows: tiles loaded as two 64-row halves
+    ("halves_c64_P3_tail", 1, 3, 192, 128, 3),
+    ("halves_c192_d64_batch2", 2, 4, 384, 64, 2),
 ]
 
 
@@ -49,9 +53,10 @@ def test_s2s_matches_oracle(case):
         compare(orc.as_f64(got), w, f"{name} partition {j}")
 
 
-@pytest.mark.parametrize("name", ["tiny", "image"])
-def test_s2s_bit_identical_to_fused_when_chunks_are_whole_tiles(name):
-    cfg = workloads.CONFIGS[name]
+@pytest.mark.parametrize("name", ["tiny", "image", "joint", "halves_c192_d64"])
+def test_s2s_bit_identical_to_fused_on_whole_or_half_tiles(name):
+    cfg = (workloads.CONFIGS[name] if name in workloads.CONFIGS
+           else workloads.AttnConfig(name, B=2, H=4, S=384, d=64, P=2))
     q, k, v = workloads.make_qkv(cfg, seed=4)
     a = bd.alloc_partitions(cfg.B, cfg.S, cfg.H, cfg.d, cfg.P)
     b = bd.alloc_partitions(cfg.B, cfg.S, cfg.H, cfg.d, cfg.P)

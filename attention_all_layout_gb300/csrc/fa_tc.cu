@@ -186,14 +186,26 @@ int launch_fa_tc_s2s(const void* const* qp, const void* const* kp, const void* c
   std::memset(&maps, 0, sizeof(maps));
   // Equal partitions whose length is a multiple of 64 but not of 128 would end
   // every partition in a half-empty block: count tiles over the whole sequence
-  // and load each as two 64-row halves instead (kModeS2SH).
-  const bool halves = epi.crem == 0 && epi.cbase % tc::kBM != 0 && epi.cbase % (tc::kBM / 2) == 0;
+  // and load each as two 64-row pieces, each inside one partition (kModeS2SG,
+  // row stores: bulk stores on top of the doubled TMA loads measured 1.6-1.9 %
+  // slower on the joint preset). Partitions of a multiple of 128 rows tile the
+  // same either way; they take the global tiles with one 128-row piece where
+  // the automatic store kind is bulk (kModeS2SGT: the image preset's layer
+  // measured 1.4 % faster than with row stores), else the per-partition tiles
+  // of kModeS2S (measured 1-2 % faster than kModeS2SG at S = 32768). Other
+  // partition lengths count tiles per partition (kModeS2S).
+  const int auto_kind = resolve_store_kind(shp.S, epi.P, true, opts.store_kind);
+  if (auto_kind == 0) return ATTN_A2A_EUNSUPPORTED;
+  const bool equal64 = epi.crem == 0 && epi.cbase > 0 && epi.cbase % (tc::kBM / 2) == 0;
+  const int seg = epi.cbase % tc::kBM == 0 ? tc::kBM : tc::kBM / 2;
+  const bool global_tiles = equal64 && (seg < tc::kBM || auto_kind == 1);
+  const int kind = seg < tc::kBM && opts.store_kind == 0 ? 2 : auto_kind;
   const long long row = static_cast<long long>(shp.H) * shp.d;  // partition j is [B, c_j, H, d]
   for (int j = 0; j < epi.P; ++j) {
     const int c = epi.cbase + (j < epi.crem ? 1 : 0);
     if (c == 0) continue;
     const long long sb = row * c;
-    const int box = halves ? tc::kBM / 2 : tc::kBM;
+    const int box = global_tiles ? seg : tc::kBM;
     if (!make_map(&maps.q[j], qp[j], shp.B, shp.H, c, shp.d, sb, shp.d, row, box) ||
         !make_map(&maps.k[j], kp[j], shp.B, shp.H, c, shp.d, sb, shp.d, row, box) ||
         !make_map(&maps.v[j], vp[j], shp.B, shp.H, c, shp.d, sb, shp.d, row, box))
@@ -201,15 +213,22 @@ int launch_fa_tc_s2s(const void* const* qp, const void* const* kp, const void* c
   }
   tc::Params p{};
   common_params(p, shp, scale, dev_status, opts);
-  if (halves) {
+  if (global_tiles) {
+    p.seg = seg;
     p.nblk = (shp.S + tc::kBM - 1) / tc::kBM;
     p.npair = (p.nblk + 1) / 2;
     p.total = shp.B * shp.H * p.npair;
     p.epi = epi;
     const int grid = grid_for(p, opts);
     if (grid <= 0) return ATTN_A2A_ECUDA;
-    if (shp.d == 128) return launch_t<128, tc::kModeS2SH, tc::kMaxS2SRanks>(maps, p, grid, stream);
-    return launch_t<64, tc::kModeS2SH, tc::kMaxS2SRanks>(maps, p, grid, stream);
+    if (kind == 1) {
+      for (int j = 0; j < epi.P; ++j)
+        if (!make_out_map(&maps.o[j], epi.part[j], shp.B, shp.H, shp.H, epi.cbase, shp.d)) return ATTN_A2A_ECUDA;
+      if (shp.d == 128) return launch_t<128, tc::kModeS2SGT, tc::kMaxS2SRanks>(maps, p, grid, stream);
+      return launch_t<64, tc::kModeS2SGT, tc::kMaxS2SRanks>(maps, p, grid, stream);
+    }
+    if (shp.d == 128) return launch_t<128, tc::kModeS2SG, tc::kMaxS2SRanks>(maps, p, grid, stream);
+    return launch_t<64, tc::kModeS2SG, tc::kMaxS2SRanks>(maps, p, grid, stream);
   }
   p.nb_big = (epi.cbase + 1 + tc::kBM - 1) / tc::kBM;
   p.nb_small = (epi.cbase + tc::kBM - 1) / tc::kBM;

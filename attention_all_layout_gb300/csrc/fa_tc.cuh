@@ -126,17 +126,29 @@ struct Cfg {
 //                waits, for the stores' shared-memory reads. A tile that
 //                straddles two partitions is stored row by row as in kModeA2A.
 //   kModeContigT as kModeContig, with the bulk-store epilogue.
-//   kModeS2SH    as kModeS2S (sequence-sharded in and out), for partitions of
-//                equal length c that is a multiple of 64 but not of 128: tiles
-//                and key blocks are counted over the whole sequence as in
-//                kModeA2A, and every 128-row tile is loaded as two 64-row halves,
-//                each lying inside one partition, so no block is half empty and
-//                the result equals kModeA2A's bit for bit. Output as kModeA2A.
-// (kModeS2S and kModeS2SH keep the row stores: with the staging path the
-// register pressure grew and the whole layer measured ≈ 3 % slower.)
-enum : int { kModeContig = 0, kModeA2A = 1, kModeS2S = 2, kModeA2AT = 3, kModeContigT = 4, kModeS2SH = 5 };
+//   kModeS2SG    as kModeS2S (sequence-sharded in and out), for partitions of
+//                equal length c, a multiple of 64: tiles and key blocks are
+//                counted over the whole sequence as in kModeA2A, and every
+//                128-row tile is loaded in p.seg-row pieces (128, or 64 when c
+//                is not a multiple of 128), each lying inside one partition, so
+//                no block is half empty and the result equals kModeA2A's bit
+//                for bit. Output as kModeA2A (row stores).
+//   kModeS2SGT   as kModeS2SG, with kModeA2AT's bulk-store epilogue.
+// (kModeS2S keeps the row stores: with the staging path its register
+// pressure grew and the whole layer measured ≈ 3 % slower.)
+enum : int {
+  kModeContig = 0,
+  kModeA2A = 1,
+  kModeS2S = 2,
+  kModeA2AT = 3,
+  kModeContigT = 4,
+  kModeS2SG = 5,
+  kModeS2SGT = 6
+};
 template <int MODE>
-constexpr bool kBulkStores = MODE == kModeA2AT || MODE == kModeContigT;
+constexpr bool kBulkStores = MODE == kModeA2AT || MODE == kModeContigT || MODE == kModeS2SGT;
+template <int MODE>
+constexpr bool kSegLoads = MODE == kModeS2SG || MODE == kModeS2SGT;
 constexpr int kMaxS2SRanks = 8;
 constexpr int kMaxStoreMaps = 8;  // output partitions with a tensor map (bulk-store epilogue)
 
@@ -158,6 +170,7 @@ struct Params {
   int store_kind;
   int nb_big, nb_small;  // kModeS2S: 128-row blocks of a longer / shorter chunk
   int interleave;        // > 1: chunk-interleaved item order with this many pairs per chunk
+  int seg;               // kModeS2SG(T): rows per TMA box of the sequence-sharded loads (128 or 64)
   EpiParams epi;
 };
 
@@ -267,22 +280,23 @@ __device__ void producer_role(const Params& p, const Maps<NMAP>* maps, uint32_t 
   uint32_t q_loads[2] = {0, 0};
   bool ok = true;
   int it = 0;
-  // kModeS2SH: rows [row, row + 128) of the sequence as two 64-row boxes, each
-  // from the partition that holds it (equal partitions of p.epi.cbase rows, a
-  // multiple of 64), into the two halves of every 128-row swizzle atom column
-  // (8 KB apart, so each half starts on a 1 KB swizzle boundary). Rows past S
-  // fall past the last partition's end and read as zeros.
-  auto load_halves = [&](uint32_t dst, const CUtensorMap* tmaps, uint32_t bar, int row, const Item& wi,
-                         uint64_t pol) {
-#pragma unroll
-    for (int hf = 0; hf < 2; ++hf) {
-      const int g = row + hf * (kBM / 2);
+  // kModeS2SG(T): rows [row, row + 128) of the sequence as 128 / p.seg boxes of
+  // p.seg rows (128, or 64), each from the partition that holds it (equal
+  // partitions of p.epi.cbase rows, a multiple of p.seg), at row offset
+  // k * p.seg of every 128-row swizzle atom column (a multiple of 8 KB, so each
+  // piece starts on a 1 KB swizzle boundary). Rows past S fall past the last
+  // partition's end and read as zeros.
+  auto load_segments = [&](uint32_t dst, const CUtensorMap* tmaps, uint32_t bar, int row, const Item& wi,
+                           uint64_t pol) {
+    for (int off = 0; off < kBM; off += p.seg) {
+      const int g = row + off;
       int j = g / p.epi.cbase;
       if (j > p.epi.P - 1) j = p.epi.P - 1;
       const int l = g - j * p.epi.cbase;
+      const uint32_t piece = dst + static_cast<uint32_t>(off) * 128u;
 #pragma unroll
       for (int a = 0; a < D / 64; ++a)
-        tma_load_4d(dst + a * C::ATOM_BYTES + hf * (C::ATOM_BYTES / 2), &tmaps[j], bar, a * 64, l, wi.h, wi.b, pol);
+        tma_load_4d(piece + a * C::ATOM_BYTES, &tmaps[j], bar, a * 64, l, wi.h, wi.b, pol);
     }
   };
   for (int item = blockIdx.x; ok && item < p.total; item += gridDim.x, ++it) {
@@ -294,8 +308,8 @@ __device__ void producer_role(const Params& p, const Maps<NMAP>* maps, uint32_t 
       int qt = 2 * wi.pair + t;  // past the last tile (odd count): rows past S read as zeros,
       if (MODE == kModeS2S && qt >= p.nblk) qt = p.nblk - 1;  // or a real tile whose rows are not stored
       const Blk bq = locate_block<MODE>(p, qt);
-      if constexpr (MODE == kModeS2SH) {
-        load_halves(dst, maps->q, BAR(C::QF + t), bq.row, wi, pol_q);
+      if constexpr (kSegLoads<MODE>) {
+        load_segments(dst, maps->q, BAR(C::QF + t), bq.row, wi, pol_q);
       } else {
 #pragma unroll
         for (int a = 0; a < D / 64; ++a)
@@ -314,8 +328,8 @@ __device__ void producer_role(const Params& p, const Maps<NMAP>* maps, uint32_t 
       if (!mbar_wait(BAR(C::KVE + s), ph ^ 1, w)) return false;
       mbar_arrive_expect_tx(BAR(C::KVF + s), C::TILE_BYTES);
       const uint32_t dst = sbase + C::KV_OFF + s * C::TILE_BYTES;
-      if constexpr (MODE == kModeS2SH) {
-        load_halves(dst, is_v ? maps->v : maps->k, BAR(C::KVF + s), bk.row, wi, pol_kv);
+      if constexpr (kSegLoads<MODE>) {
+        load_segments(dst, is_v ? maps->v : maps->k, BAR(C::KVF + s), bk.row, wi, pol_kv);
       } else {
 #pragma unroll
         for (int a = 0; a < D / 64; ++a)
@@ -526,7 +540,7 @@ __device__ __forceinline__ float probs(const uint32_t (&sr)[128], uint32_t (&pk)
   return s0 + s1;
 }
 
-// Bulk-store epilogue of one tile (kModeA2AT): the 128 owner threads write
+// Bulk-store epilogue of one tile (kModeA2AT, kModeS2SGT): the 128 owner threads write
 // their normalised bf16 rows into the staging buffer (128-byte swizzle, as
 // the tensor map expects), hand them to the async proxy, and one elected
 // thread issues the tile's tensor stores through output map `map` at
@@ -746,8 +760,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    const int nmaps = MODE == kModeS2S || MODE == kModeS2SH ? p.epi.P : 1;
-    if (MODE == kModeA2AT)
+    const int nmaps = MODE == kModeS2S || kSegLoads<MODE> ? p.epi.P : 1;
+    if (MODE == kModeA2AT || MODE == kModeS2SGT)
       for (int i = 0; i < p.epi.P && i < kMaxStoreMaps; ++i)
         if (p.epi.cbase > 0 || i < p.epi.crem) tma_prefetch_desc(&maps.o[i]);  // partitions with rows only
     if (MODE == kModeContigT) tma_prefetch_desc(&maps.o[0]);

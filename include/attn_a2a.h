@@ -155,10 +155,13 @@ int attn_a2a_fwd_contig_ex(const void* q, const void* k, const void* v,
  *   shp            : B, H, S (= sum of c_j), d; the strides are ignored.
  *   P              : 1 <= P <= 8 (ATTN_A2A_EUNSUPPORTED beyond), H % P == 0.
  *   out_partitions : as for attn_a2a_fwd.
- * Query tiles and key blocks are taken per partition (each starts at a
- * partition's first row), so when c_j is not a multiple of 128 the key
- * blocks differ from attn_a2a_fwd's and the rounding may differ in the last
- * bits; for c_j a multiple of 128 both calls are bit-identical.
+ * When all partitions have the same length and it is a multiple of 64 rows,
+ * query tiles and key blocks are counted over the whole sequence and each
+ * 128-row tile is loaded in pieces that lie inside one partition (one piece,
+ * or two 64-row halves); the result is then bit-identical to attn_a2a_fwd's.
+ * Otherwise tiles and key blocks are taken per partition (each starting at a
+ * partition's first row), so the key blocks differ from attn_a2a_fwd's and
+ * the rounding may differ in the last bits.
  */
 int attn_a2a_fwd_s2s(const void* const* q_parts, const void* const* k_parts,
                      const void* const* v_parts, const attn_a2a_shape* shp, int P, float scale,

@@ -53,10 +53,16 @@ def test_s2s_matches_oracle(case):
         compare(orc.as_f64(got), w, f"{name} partition {j}")
 
 
-@pytest.mark.parametrize("name", ["tiny", "image", "joint", "halves_c192_d64"])
+EXTRA = {
+    "halves_c192_d64": dict(B=2, H=4, S=384, d=64, P=2),
+    # whole-tile partitions past S = 16384: row stores, per-partition tiles
+    "whole_c8320_rows": dict(B=1, H=2, S=16640, d=128, P=2),
+}
+
+
+@pytest.mark.parametrize("name", ["tiny", "image", "joint", "halves_c192_d64", "whole_c8320_rows"])
 def test_s2s_bit_identical_to_fused_on_whole_or_half_tiles(name):
-    cfg = (workloads.CONFIGS[name] if name in workloads.CONFIGS
-           else workloads.AttnConfig(name, B=2, H=4, S=384, d=64, P=2))
+    cfg = workloads.CONFIGS[name] if name in workloads.CONFIGS else workloads.AttnConfig(name, **EXTRA[name])
     q, k, v = workloads.make_qkv(cfg, seed=4)
     a = bd.alloc_partitions(cfg.B, cfg.S, cfg.H, cfg.d, cfg.P)
     b = bd.alloc_partitions(cfg.B, cfg.S, cfg.H, cfg.d, cfg.P)

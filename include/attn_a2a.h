@@ -308,7 +308,8 @@ const char* attn_a2a_strerror(int status);
  * (0 if no device). Host-only query, no launch. */
 int attn_a2a_num_sms(void);
 
-/* The store kind (attn_a2a_opts.store_kind) a call would use for its output
+/* The store kind (attn_a2a_opts.store_kind) an attn_a2a_fwd(_ex) (layout 1)
+ * or attn_a2a_fwd_contig(_ex) (layout 0) call would use for its output
  * tiles: 1 = bulk tensor stores from a staging tile, 2 = row stores from
  * registers. S = sequence length, P = partitions (1 for the contiguous
  * layout), layout = 0 contiguous ("attention alone"), 1 all-to-all;

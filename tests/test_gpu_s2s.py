@@ -34,6 +34,9 @@ CASES = [
     # equal chunks of 64 (mod 128) rows: tiles loaded as two 64-row halves
     ("halves_c64_P3_tail", 1, 3, 192, 128, 3),
     ("halves_c192_d64_batch2", 2, 4, 384, 64, 2),
+    # one partition: the layer is attention in the sequence-major layout
+    ("P1_halves_c320", 1, 2, 320, 128, 1),
+    ("P1_whole_c256_d64", 1, 2, 256, 64, 1),
 ]
 
 

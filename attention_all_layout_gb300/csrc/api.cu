@@ -100,15 +100,42 @@ bool partitions_alias_inputs(const attn_a2a_shape& shp, const EpiParams& e, cons
 
 // Copy streams and events of the host-buffer entry point, created once per
 // device on first use (host-side resources; no device memory).
-constexpr int kHostChunks = 4;
+constexpr int kMaxHostChunks = 8;
 
 struct HostPipe {
   std::once_flag once;
   std::mutex mu;
   bool ok = false;
-  cudaStream_t h2d = nullptr, d2h = nullptr;
+  cudaStream_t h2d = nullptr, d2h = nullptr, comp2 = nullptr;
   cudaEvent_t ev_start = nullptr, ev_h2d = nullptr, ev_comp = nullptr, ev_end = nullptr;
 };
+
+// Head counts of the chunks of one batch entry of the host-buffer call. The
+// first chunk is small, so that little copying is exposed before the first
+// kernel; each next chunk grows by at most 2.5x, so that its copy (about a
+// third of its kernel's time per head at ~200 GB/s) finishes while the kernel
+// before it runs; the last chunk is small again, so that little copying back
+// is exposed after the last kernel. Returns the number of chunks (<= kMaxHostChunks).
+int plan_head_chunks(int H, int* chunk) {
+  if (H <= 4) {
+    for (int i = 0; i < H; ++i) chunk[i] = 1;
+    return H;
+  }
+  const int first = H / 16 > 1 ? H / 16 : 1;
+  int n = 0, rem = H, prev = first;
+  chunk[n++] = first;
+  rem -= first;
+  while (rem > first && n < kMaxHostChunks - 1) {
+    int next = (5 * prev + 1) / 2;                  // at most 2.5x the previous chunk
+    if (next > rem - first) next = rem - first;     // leave a small last chunk
+    if (n == kMaxHostChunks - 2) next = rem - first;
+    chunk[n++] = next;
+    rem -= next;
+    prev = next;
+  }
+  chunk[n++] = rem;
+  return n;
+}
 
 HostPipe g_pipes[128];
 
@@ -120,6 +147,7 @@ HostPipe* host_pipe() {
     const unsigned ef = cudaEventDisableTiming;
     hp->ok = cudaStreamCreateWithFlags(&hp->h2d, cudaStreamNonBlocking) == cudaSuccess &&
              cudaStreamCreateWithFlags(&hp->d2h, cudaStreamNonBlocking) == cudaSuccess &&
+             cudaStreamCreateWithFlags(&hp->comp2, cudaStreamNonBlocking) == cudaSuccess &&
              cudaEventCreateWithFlags(&hp->ev_start, ef) == cudaSuccess &&
              cudaEventCreateWithFlags(&hp->ev_h2d, ef) == cudaSuccess &&
              cudaEventCreateWithFlags(&hp->ev_comp, ef) == cudaSuccess &&
@@ -318,18 +346,24 @@ int attn_a2a_fwd_host(const void* hq, const void* hk, const void* hv, const attn
   if (hp == nullptr) return ATTN_A2A_ECUDA;
   std::lock_guard<std::mutex> lock(hp->mu);
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // Heads are processed in chunks: the host->device copy of the next chunk and
-  // the device->host copy of the previous one overlap the kernel of this one.
-  const int nchunk = s.H < kHostChunks ? s.H : kHostChunks;
-  const int hc = (s.H + nchunk - 1) / nchunk;
+  // Heads are processed in chunks (plan_head_chunks): the host->device copy
+  // of the next chunk and the device->host copy of the previous one overlap
+  // the kernel of this one, and consecutive chunks' kernels alternate between
+  // the caller's stream and a second one, so that the next kernel's CTAs take
+  // the SMs the last wave of the previous one leaves idle.
+  int chunk[kMaxHostChunks];
+  const int nchunk = plan_head_chunks(s.H, chunk);
   const size_t head_elems = static_cast<size_t>(s.S) * s.d;
   // device buffers may still be in use by earlier work on the caller's stream
-  if (cudaEventRecord(hp->ev_start, st) != cudaSuccess || cudaStreamWaitEvent(hp->h2d, hp->ev_start, 0) != cudaSuccess)
+  if (cudaEventRecord(hp->ev_start, st) != cudaSuccess || cudaStreamWaitEvent(hp->h2d, hp->ev_start, 0) != cudaSuccess ||
+      cudaStreamWaitEvent(hp->comp2, hp->ev_start, 0) != cudaSuccess)
     return ATTN_A2A_ECUDA;
   const attn_a2a_opts o = default_opts();
+  int launch = 0;
   for (int b = 0; b < s.B; ++b) {
-    for (int h0 = 0; h0 < s.H; h0 += hc) {
-      const int h1 = h0 + hc < s.H ? h0 + hc : s.H;
+    for (int ci = 0, h0 = 0; ci < nchunk; h0 += chunk[ci], ++ci, ++launch) {
+      const int h1 = h0 + chunk[ci];
+      const cudaStream_t cs_stream = launch % 2 == 0 ? st : hp->comp2;
       const size_t off = (static_cast<size_t>(b) * s.H + h0) * head_elems;  // elements
       const size_t bytes = static_cast<size_t>(h1 - h0) * head_elems * 2u;
       const void* hsrc[3] = {hq, hk, hv};
@@ -338,7 +372,8 @@ int attn_a2a_fwd_host(const void* hq, const void* hk, const void* hv, const attn
         if (cudaMemcpyAsync(static_cast<uint16_t*>(ddst[i]) + off, static_cast<const uint16_t*>(hsrc[i]) + off, bytes,
                             cudaMemcpyHostToDevice, hp->h2d) != cudaSuccess)
           return ATTN_A2A_ECUDA;
-      if (cudaEventRecord(hp->ev_h2d, hp->h2d) != cudaSuccess || cudaStreamWaitEvent(st, hp->ev_h2d, 0) != cudaSuccess)
+      if (cudaEventRecord(hp->ev_h2d, hp->h2d) != cudaSuccess ||
+          cudaStreamWaitEvent(cs_stream, hp->ev_h2d, 0) != cudaSuccess)
         return ATTN_A2A_ECUDA;
       attn_a2a_shape cs = s;  // one batch entry, heads [h0, h1)
       cs.B = 1;
@@ -352,9 +387,10 @@ int attn_a2a_fwd_host(const void* hq, const void* hk, const void* hv, const attn
                            : nullptr;
       }
       rc = launch_fa_tc(static_cast<uint16_t*>(dq) + off, static_cast<uint16_t*>(dk) + off,
-                        static_cast<uint16_t*>(dv) + off, cs, scale, true, ce, dev_status, o, st);
+                        static_cast<uint16_t*>(dv) + off, cs, scale, true, ce, dev_status, o, cs_stream);
       if (rc != ATTN_A2A_OK) return rc;
-      if (cudaEventRecord(hp->ev_comp, st) != cudaSuccess || cudaStreamWaitEvent(hp->d2h, hp->ev_comp, 0) != cudaSuccess)
+      if (cudaEventRecord(hp->ev_comp, cs_stream) != cudaSuccess ||
+          cudaStreamWaitEvent(hp->d2h, hp->ev_comp, 0) != cudaSuccess)
         return ATTN_A2A_ECUDA;
       for (int j = 0; j < P; ++j) {
         const int c = epi.cbase + (j < epi.crem ? 1 : 0);
@@ -369,7 +405,8 @@ int attn_a2a_fwd_host(const void* hq, const void* hk, const void* hv, const attn
       }
     }
   }
-  // the caller's stream completes only when the last copy back has
+  // the caller's stream completes only when the last copy back has (which
+  // follows every chunk's kernel, on either stream)
   if (cudaEventRecord(hp->ev_end, hp->d2h) != cudaSuccess || cudaStreamWaitEvent(st, hp->ev_end, 0) != cudaSuccess)
     return ATTN_A2A_ECUDA;
   return ATTN_A2A_OK;

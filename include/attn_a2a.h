@@ -191,11 +191,15 @@ int attn_a2a_fwd_simt(const void* q, const void* k, const void* v, const attn_a2
  * pinned for asynchronous copies) into the caller's device buffers dq, dk,
  * dv, runs the fused attention into the caller's device partitions dparts[j],
  * and copies each partition back into hparts[j] (host). The heads are
- * processed in up to four chunks so that the copies of one chunk overlap the
- * kernel of another; the copies run on two library-owned streams (created,
- * with four events, on the first call per device) ordered by events against
- * `stream`: they start after the work already queued on `stream`, and
- * `stream` completes only after the last copy back. Returns after enqueueing;
+ * processed in up to eight chunks - small first and last ones, so that
+ * little copying is exposed before the first kernel and after the last - so
+ * that the copies of one chunk overlap the kernel of another; the copies run
+ * on two library-owned streams, and the chunks' kernels alternate between
+ * `stream` and a third library-owned stream so that one kernel's last wave
+ * overlaps the next kernel (the streams and four events are created on the
+ * first call per device). Everything is ordered by events against `stream`:
+ * it starts after the work already queued on `stream`, and `stream`
+ * completes only after the last copy back. Returns after enqueueing;
  * synchronise `stream` before reading hparts. Calls on one device are
  * serialised while they enqueue.
  */

@@ -142,8 +142,11 @@ def test_empty_sequence_launches_nothing():
     assert bd.attn_a2a_fwd(q, q, q, 2, 0.1, [None, None]) == bd.OK
 
 
-def test_host_entry_point_matches_device_path():
-    cfg = workloads.config("image", H=4, S=1500)
+@pytest.mark.parametrize("B,H,S", [(1, 4, 1500), (2, 16, 640), (1, 40, 300)])
+def test_host_entry_point_matches_device_path(B, H, S):
+    # head chunks: one head each for H = 4; a ramp (1, 3, 8, 3, 1 heads) per
+    # batch entry for H = 16; the video head count (2, 5, 13, 18, 2) for H = 40
+    cfg = workloads.config("image", B=B, H=H, S=S)
     q, k, v = workloads.make_qkv(cfg, seed=5)
     hq, hk, hv = (t.pin_memory() for t in (q, k, v))
     dq, dk, dv = (torch.empty_like(t, device="cuda") for t in (q, k, v))

@@ -79,3 +79,48 @@ def test_full_size_sampled_rows_and_layout(name):
         assert np.all(np.abs(got - want) <= abs_tolerance(want)), f"{name} head {h}: max|err| {err:.3e}"
         assert rf <= REL_FRO, f"{name} head {h}: rel-Frobenius {rf:.3e}"
     print(f"{name}: {len(rows)} rows x {cfg.H} heads, max|err| {worst_abs:.3e}, worst rel-Fro {worst_rf:.3e}")
+
+
+def _seq_shards(t, P):
+    """[B, H, S, d] device tensor -> P contiguous [B, c_j, H, d] partitions (test-side data prep)."""
+    out, start = [], 0
+    for c in bd.chunk_sizes(t.shape[2], P):
+        out.append(t[:, :, start:start + c].permute(0, 2, 1, 3).contiguous())
+        start += c
+    return out
+
+
+@pytest.mark.parametrize("name", ["video", "long"])
+def test_full_size_whole_layer(name):
+    # the whole Ulysses layer (sequence-sharded q, k, v in) at full size: the
+    # video preset's whole-tile partitions give the fused call's bytes; the
+    # long preset's ragged partitions (9450 rows) are tiled per partition, so
+    # they are checked against the oracle on sampled rows of a few heads
+    cfg = workloads.CONFIGS[name]
+    q, k, v = workloads.make_qkv(cfg, seed=0)
+    dq, dk, dv = q.cuda(), k.cuda(), v.cuda()
+    g = GuardedPartitions(cfg.B, cfg.S, cfg.H, cfg.d, cfg.P)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    bd.attn_a2a_fwd_s2s(_seq_shards(dq, cfg.P), _seq_shards(dk, cfg.P), _seq_shards(dv, cfg.P), cfg.P, cfg.scale,
+                        g.parts, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert g.guards_intact()
+    if name == "video":
+        ref = bd.alloc_partitions(cfg.B, cfg.S, cfg.H, cfg.d, cfg.P)
+        bd.attn_a2a_fwd(dq, dk, dv, cfg.P, cfg.scale, ref)
+        torch.cuda.synchronize()
+        for a, b in zip(g.parts, ref):
+            assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+        return
+    rows, _ = sample_rows(cfg.S, cfg.P, seed=8)
+    bounds = orc.chunk_bounds(cfg.S, cfg.P)
+    host_parts = [p.cpu() for p in g.parts]
+    for h in (0, 17, cfg.H - 1):
+        want = orc.attention_rows_fp64(q, k, v, cfg.scale, 0, h, rows)
+        got = np.empty_like(want)
+        for i, s in enumerate(rows):
+            j = next(jj for jj, (st, c) in enumerate(bounds) if st <= s < st + c)
+            got[i] = orc.as_f64(host_parts[j][0, s - bounds[j][0], h])
+        assert np.all(np.abs(got - want) <= abs_tolerance(want)), f"{name} head {h}"
+        assert rel_fro(got, want) <= REL_FRO, f"{name} head {h}"

@@ -119,7 +119,6 @@ void common_params(tc::Params& p, const attn_a2a_shape& shp, float scale, int* d
   p.dev_status = dev_status;
   p.timeout_ns = opts.timeout_ns > 0 ? static_cast<unsigned long long>(opts.timeout_ns) : 2000000000ull;
   p.inject_stall = opts.inject_stall;
-  p.store_kind = opts.store_kind;
 }
 
 int grid_for(const tc::Params& p, const attn_a2a_opts& opts) {

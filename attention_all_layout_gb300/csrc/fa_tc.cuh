@@ -167,7 +167,6 @@ struct Params {
   int* dev_status;
   unsigned long long timeout_ns;
   int inject_stall;
-  int store_kind;
   int nb_big, nb_small;  // kModeS2S: 128-row blocks of a longer / shorter chunk
   int interleave;        // > 1: chunk-interleaved item order with this many pairs per chunk
   int seg;               // kModeS2SG(T): rows per TMA box of the sequence-sharded loads (128 or 64)

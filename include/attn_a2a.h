@@ -30,8 +30,10 @@
  *
  * Conventions shared by every entry point:
  *   - Ownership: the caller owns every buffer. The library allocates no
- *     device memory; it keeps small host-side state only (a cached driver
- *     entry point and the SM count per device).
+ *     device memory per call; it keeps small host-side state only (a cached
+ *     driver entry point, the SM count per device, and the streams and
+ *     events of attn_a2a_fwd_host), plus the fixed __device__ array of
+ *     xstage_probe_run_noalloc.
  *   - Streams: `stream` is a cudaStream_t passed as void* (NULL = the legacy
  *     default stream). Work is asynchronous on that stream.
  *   - Errors: argument errors are detected on the host and returned

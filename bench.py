@@ -12,7 +12,8 @@ Prints one JSON line. Legs:
                fused kernel, partitions -> pinned host) timed end to end
   roofline     the fused kernel against the measured bf16 tensor peak
   cpu_baseline the float64 oracle on a bounded row sample, on host cores
-  attention-alone and serial (attention, then a separate permute) times
+  attention-alone, serial (attention, then a separate permute) and whole-layer
+               times, taken in turns with the fused call over three rounds
 `--impl reference` times the oracle arm instead (CPU, rank 0 only).
 Multi-GPU (torchrun): every rank runs an independent replica of the workload
 (no data-path collective); value is the sum over ranks / slowest rank's time.
@@ -360,20 +361,31 @@ def main():
                                          "d": cfg.d, "P": cfg.P}, "clocks": clocks, "fused_only": True}),
                   flush=True)
         return 0
-    # ---- attention alone and the serial baseline (same kernel, contiguous epilogue)
-    ms_contig = time_events(contig, max(5, args.steps // 3), 2, stream)
-    ms_permute = time_events(lambda: bd.attn_a2a_permute(o, cfg.P, parts, stream=stream),
-                             max(5, args.steps // 3), 2, stream)
-    ms_serial = time_events(serial, max(5, args.steps // 3), 2, stream)
-
-    # ---- the whole Ulysses layer: sequence-sharded q, k, v in (pre-attention
-    # exchange folded into the loads), sequence-sharded output out
-    ms_s2s = None
+    # ---- comparison legs, taking turns over three rounds (median per leg), so
+    # that a clock drift under the power cap does not favour the leg timed
+    # first: the fused call again, attention alone and the serial baseline
+    # (same kernel, contiguous epilogue, then the separate permute), and the
+    # whole Ulysses layer (sequence-sharded q, k, v in: the pre-attention
+    # exchange folded into the loads; sequence-sharded output out)
+    legs = {
+        "fused": fused,
+        "contig": contig,
+        "permute": lambda: bd.attn_a2a_permute(o, cfg.P, parts, stream=stream),
+        "serial": serial,
+    }
     if cfg.P <= 8:
         sq, sk, sv = ([t[:, :, st:st + c].permute(0, 2, 1, 3).contiguous()
                        for st, c in zip(_starts(cfg.S, cfg.P), bd.chunk_sizes(cfg.S, cfg.P))] for t in (q, k, v))
-        ms_s2s = time_events(lambda: bd.attn_a2a_fwd_s2s(sq, sk, sv, cfg.P, cfg.scale, parts, dev_status=status,
-                                                         stream=stream), max(5, args.steps // 3), 2, stream)
+        legs["s2s"] = lambda: bd.attn_a2a_fwd_s2s(sq, sk, sv, cfg.P, cfg.scale, parts, dev_status=status,
+                                                  stream=stream)
+    turns = {name: [] for name in legs}
+    for _ in range(3):
+        for name, fn in legs.items():
+            turns[name].append(time_events(fn, max(5, args.steps // 3), 1, stream))
+    med = {name: statistics.median(v) for name, v in turns.items()}
+    ms_turns, ms_contig, ms_permute, ms_serial = med["fused"], med["contig"], med["permute"], med["serial"]
+    ms_s2s = med.get("s2s")
+    if cfg.P <= 8:
         del sq, sk, sv
 
     # ---- e2e: host buffers through the C-ABI host entry point
@@ -444,11 +456,12 @@ def main():
         "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
                      "frac": tflops / peak, "traffic": traffic,
                      "kernel": fused_kernel_label(cfg), "peak_source": f"{peak_src} bf16_tflops (burst)"},
+        "fused_in_turns_ms": ms_turns,
         "attention_alone_ms": ms_contig,
         "permute_ms": ms_permute,
         "serial_ms": ms_serial,
-        "epilogue_overhead": ms / ms_contig - 1.0,
-        "speedup_vs_serial": ms_serial / ms,
+        "epilogue_overhead": ms_turns / ms_contig - 1.0,
+        "speedup_vs_serial": ms_serial / ms_turns,
         "ulysses_layer_s2s_ms": ms_s2s,
         "ulysses_layer_s2s_tflops": (flops / (ms_s2s * 1e-3) / 1e12) if ms_s2s else None,
         "e2e": {"value": flops / (ms_e2e * 1e-3) / 1e12 * world, "unit": "TFLOP/s",

@@ -121,7 +121,7 @@ int plan_head_chunks(int H, int* chunk) {
     for (int i = 0; i < H; ++i) chunk[i] = 1;
     return H;
   }
-  const int first = H / 16 > 1 ? H / 16 : 1;
+  const int first = H / 32 > 1 ? H / 32 : 1;
   int n = 0, rem = H, prev = first;
   chunk[n++] = first;
   rem -= first;

@@ -145,7 +145,7 @@ def test_empty_sequence_launches_nothing():
 @pytest.mark.parametrize("B,H,S", [(1, 4, 1500), (2, 16, 640), (1, 40, 300)])
 def test_host_entry_point_matches_device_path(B, H, S):
     # head chunks: one head each for H = 4; a ramp (1, 3, 8, 3, 1 heads) per
-    # batch entry for H = 16; the video head count (2, 5, 13, 18, 2) for H = 40
+    # batch entry for H = 16; the video head count (1, 3, 8, 20, 7, 1) for H = 40
     cfg = workloads.config("image", B=B, H=H, S=S)
     q, k, v = workloads.make_qkv(cfg, seed=5)
     hq, hk, hv = (t.pin_memory() for t in (q, k, v))

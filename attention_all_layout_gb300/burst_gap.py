@@ -14,7 +14,7 @@ The probe kernel (``xstage_probe_run``) records three %globaltimer stamps per
 producer and round; everything here is arithmetic on those stamps.
 Here stores go to local HBM, so R is the local store-drain rate.
 
-Fitting (this build's procedure; the pages give none):
+Fitting (the pages give no procedure; this one is our own):
   * T0(K, V): median issue time of rounds whose gap is long enough that the
     previous burst has drained (the largest G measured for that K, V);
   * R: from the drain-dominated points, where the steady-state period
@@ -24,7 +24,7 @@ Fitting (this build's procedure; the pages give none):
     in V, until one burst overflows the capacity; past the knee the floor is
     (V - Q) / R. The line through the two smallest volumes extrapolates the
     issue-limited time; for volumes whose floor exceeds it by 25 % or more,
-    Q = V - R * floor. (This reading of Q is this build's; the pages' equation
+    Q = V - R * floor. (This reading of Q is our own; the pages' equation
     does not contain Q.)
 """
 from __future__ import annotations

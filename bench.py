@@ -429,9 +429,11 @@ def main():
     if not args.no_cpu_baseline:
         cores = os.cpu_count() or 1
         torch.set_num_threads(cores)
-        val, nrows, secs = cpu_oracle_sample(q, k, v, cfg, rows_per_head=256, heads=cfg.H, seed=0)
+        # a bounded sample: about 10-15 s of float64 work on the host's cores
+        rows_per_head = 1024
+        val, nrows, secs = cpu_oracle_sample(q, k, v, cfg, rows_per_head=rows_per_head, heads=cfg.H, seed=0)
         cpu = {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-               "sample": f"{nrows} query rows (256 random rows x {cfg.H} heads) of this workload at full key "
+               "sample": f"{nrows} query rows ({rows_per_head} random rows x {cfg.H} heads) of this workload at full key "
                          f"length, float64 numpy oracle incl. the row's layout destination; "
                          f"{secs:.1f} s of CPU work; TFLOP/s = 4*S*d per row / time"}
     line = {

@@ -21,7 +21,7 @@ Overlap in DiT Inference, gist.science explanation, Technical Summary,
 Units: seconds, bytes and bytes/second (any consistent set works).
 
 The equation does not contain Q. ``t_iss_with_capacity`` and
-``fluid_queue_rounds`` are this build's reading of where Q enters, stated as a
+``fluid_queue_rounds`` are a reading of where Q enters, stated as a
 derivation of our own and checked against the equation where the two must
 agree: the X-stage is a fluid queue of capacity Q drained at R; the producer
 issues at rate V/T0 while the queue has room and at R once it is full; during

@@ -1,7 +1,7 @@
 """CPU oracle of the synthetic MegaMoE-style grouped GEMM with scattered
 outputs (test infrastructure only; shares no code with the CUDA path).
 
-Definition (this build's synthetic stand-in for the pages' MegaMoE
+Definition (our own synthetic stand-in for the pages' MegaMoE
 workload, X-Stage explanation, "Key Contributions", MegaMoE reshaping): for a
 task (kind, e, m, n) the output tile is rows [128m, 128m+128) and columns
 [256n, 256n+256) of x[e] @ w^T with w = w1[e] for kind 0 and w2[e] for kind

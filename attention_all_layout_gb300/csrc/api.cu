@@ -437,13 +437,9 @@ int moe_gemm_scatter(const void* x, const void* w1, const void* w2, int E, int T
 int xstage_probe_run(const xstage_probe_cfg* cfg, void* stream) {
   if (cfg == nullptr) return ATTN_A2A_EINVAL;
   const xstage_probe_cfg& c = *cfg;
-  if (c.K < 1 || c.K > 1024 || c.rounds < 1) return ATTN_A2A_EINVAL;
-  if (c.V_bytes <= 0 || c.V_bytes % (4096ll * c.K) != 0) return ATTN_A2A_EINVAL;
+  const int bad = check_probe_cfg(c);
+  if (bad != ATTN_A2A_OK) return bad;
   if (c.dst_bytes < c.V_bytes || c.dst == nullptr || !aligned16(c.dst)) return ATTN_A2A_EINVAL;
-  if (c.G_ns < 0 || c.store_kind < 0 || c.store_kind > 1 || c.gap_kind < 0 || c.gap_kind > 2)
-    return ATTN_A2A_EINVAL;
-  if (c.gap_kind >= 1 && (c.fma_iters < 0 || c.fma_iters > 100000000ll)) return ATTN_A2A_EINVAL;
-  if (c.stamps == nullptr || (reinterpret_cast<uintptr_t>(c.stamps) & 7u) != 0) return ATTN_A2A_EINVAL;
   return launch_probe(c, static_cast<cudaStream_t>(stream));
 }
 

@@ -39,6 +39,14 @@ int launch_fa_simt(const void* q, const void* k, const void* v, const attn_a2a_s
 int launch_permute(const void* o, const attn_a2a_shape& shp, const EpiParams& epi,
                    cudaStream_t stream);
 
+// Upper bound of xstage_probe_cfg.fma_iters (gap_kind 1 and 2), so that no
+// probe holds the GPU for long.
+constexpr long long kProbeMaxGapIters = 100000000ll;
+
+// Argument checks of the probe entry points, apart from the burst target:
+// ATTN_A2A_OK or ATTN_A2A_EINVAL.
+int check_probe_cfg(const xstage_probe_cfg& cfg);
+
 int launch_probe(const xstage_probe_cfg& cfg, cudaStream_t stream);
 
 int launch_moe_gemm(const void* x, const void* w1, const void* w2, int E, int T, int K, int N,

@@ -152,24 +152,45 @@ int launch_probe(const xstage_probe_cfg& c, cudaStream_t stream) {
   return cudaGetLastError() == cudaSuccess ? ATTN_A2A_OK : ATTN_A2A_ECUDA;
 }
 
+// Field checks shared by both probe entry points (everything except the
+// caller's burst target, which only xstage_probe_run takes).
+int check_probe_cfg(const xstage_probe_cfg& c) {
+  if (c.K < 1 || c.K > 1024 || c.rounds < 1) return ATTN_A2A_EINVAL;
+  if (c.V_bytes <= 0 || c.V_bytes % (4096ll * c.K) != 0) return ATTN_A2A_EINVAL;
+  if (c.G_ns < 0 || c.store_kind < 0 || c.store_kind > 1 || c.gap_kind < 0 || c.gap_kind > 2)
+    return ATTN_A2A_EINVAL;
+  if (c.gap_kind >= 1 && (c.fma_iters < 0 || c.fma_iters > kProbeMaxGapIters)) return ATTN_A2A_EINVAL;
+  if (c.stamps == nullptr || (reinterpret_cast<uintptr_t>(c.stamps) & 7u) != 0) return ATTN_A2A_EINVAL;
+  return ATTN_A2A_OK;
+}
+
 namespace {
 
 constexpr int kMaxDevices = 64;
-std::once_flag g_noalloc_once[kMaxDevices];
+std::mutex g_noalloc_mu;
 void* g_noalloc_ptr[kMaxDevices];
-cudaError_t g_noalloc_err[kMaxDevices];
 
 // Device address of g_noalloc_target on the current device. In host code the
 // array's name is only a host-side stand-in, not an address a kernel may use;
-// the usable address comes from cudaGetSymbolAddress, looked up once per device
-// with that device current (the first call on each device does this set-up).
+// the usable address comes from cudaGetSymbolAddress, looked up with that
+// device current by the first call on each device. Only a successful lookup
+// is kept: after a failure the call returns ATTN_A2A_ECUDA and the next call
+// tries again.
 int noalloc_target(void** out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_A2A_ECUDA;
-  std::call_once(g_noalloc_once[dev], [dev] {
-    g_noalloc_err[dev] = cudaGetSymbolAddress(&g_noalloc_ptr[dev], g_noalloc_target);
-  });
-  if (g_noalloc_err[dev] != cudaSuccess || g_noalloc_ptr[dev] == nullptr) return ATTN_A2A_ECUDA;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();  // leave no stale error for the next launch check
+    return ATTN_A2A_ECUDA;
+  }
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_target) != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      return ATTN_A2A_ECUDA;
+    }
+    g_noalloc_ptr[dev] = p;
+  }
   *out = g_noalloc_ptr[dev];
   return ATTN_A2A_OK;
 }
@@ -177,27 +198,22 @@ int noalloc_target(void** out) {
 }  // namespace
 }  // namespace attn_a2a
 
-// The probe without any device allocation: same kernel, burst target in the
-// library's fixed array instead of a caller buffer. No cudaMalloc, cudaFree or
-// allocating library call is made here.
+// The probe without any device allocation: the same checks and the same
+// launch as xstage_probe_run, with the burst target in the library's fixed
+// array instead of a caller buffer. No cudaMalloc, cudaFree or allocating
+// library call is made here (cudaFuncSetAttribute, which gap_kind 2 and the
+// bulk-copy source need for their shared memory, allocates nothing).
 extern "C" int xstage_probe_run_noalloc(const xstage_probe_cfg* cfg, void* stream) {
   using namespace attn_a2a;
   if (cfg == nullptr) return ATTN_A2A_EINVAL;
-  const xstage_probe_cfg& c = *cfg;
-  if (c.K < 1 || c.K > 1024 || c.rounds < 1) return ATTN_A2A_EINVAL;
-  if (c.V_bytes <= 0 || c.V_bytes % (4096ll * c.K) != 0) return ATTN_A2A_EINVAL;
-  if (c.V_bytes > XSTAGE_PROBE_NOALLOC_MAX_BYTES) return ATTN_A2A_ETOOLARGE;
-  if (c.G_ns < 0 || c.store_kind < 0 || c.store_kind > 1 || c.gap_kind < 0 || c.gap_kind > 1)
-    return ATTN_A2A_EINVAL;
-  if (c.gap_kind == 1 && c.fma_iters < 0) return ATTN_A2A_EINVAL;
-  if (c.stamps == nullptr || (reinterpret_cast<uintptr_t>(c.stamps) & 7u) != 0) return ATTN_A2A_EINVAL;
+  const int bad = check_probe_cfg(*cfg);
+  if (bad != ATTN_A2A_OK) return bad;
+  if (cfg->V_bytes > XSTAGE_PROBE_NOALLOC_MAX_BYTES) return ATTN_A2A_ETOOLARGE;
   void* target = nullptr;
   const int rc = noalloc_target(&target);
   if (rc != ATTN_A2A_OK) return rc;
-  // the bulk-copy source (32 KB) is within the default dynamic shared-memory limit
-  const int smem = c.store_kind == 1 ? kBulkChunk : 0;
-  xstage_probe_kernel<<<c.K, kProbeThreads, smem, static_cast<cudaStream_t>(stream)>>>(
-      static_cast<uint8_t*>(target), XSTAGE_PROBE_NOALLOC_MAX_BYTES, c.V_bytes, c.rounds, c.G_ns,
-      c.store_kind, c.gap_kind, c.fma_iters, c.stamps);
-  return cudaGetLastError() == cudaSuccess ? ATTN_A2A_OK : ATTN_A2A_ECUDA;
+  xstage_probe_cfg c = *cfg;
+  c.dst = target;
+  c.dst_bytes = XSTAGE_PROBE_NOALLOC_MAX_BYTES;
+  return launch_probe(c, static_cast<cudaStream_t>(stream));
 }

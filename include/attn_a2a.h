@@ -262,10 +262,17 @@ int xstage_probe_run(const xstage_probe_cfg* cfg, void* stream);
  * is smaller than L2, this variant measures stores absorbed by L2, not the
  * drain into HBM that a large caller-owned target measures.
  *
+ * Argument checks are those of xstage_probe_run (same status for the same
+ * fields, including the fma_iters bound and gap_kind 2), apart from dst.
+ *
  * Set-up: the first call on each device looks up the device address of the
  * array (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture. The call allocates nothing (no cudaMalloc,
- * cudaFree or allocating library routine).
+ * before any stream capture. Only a successful lookup is kept: if it fails,
+ * the call returns ATTN_A2A_ECUDA and the next call on that device tries
+ * again. The call allocates nothing (no cudaMalloc, cudaFree or allocating
+ * library routine); like xstage_probe_run it raises the kernel's dynamic
+ * shared-memory limit with cudaFuncSetAttribute for store_kind 1 and
+ * gap_kind 2, which allocates nothing either.
  *
  * Sharing: all calls on a device use the same array and it keeps the last
  * call's contents. The probe only writes it, so nothing has to start at zero.

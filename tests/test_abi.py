@@ -172,7 +172,35 @@ def test_noalloc_probe_validation(lib):
     assert run(K=0) == bd.EINVAL
     assert run(stamps=0) == bd.EINVAL
     assert run(store_kind=3) == bd.EINVAL
+    assert run(gap_kind=1, fma_iters=10**8 + 1) == bd.EINVAL
+    assert run(gap_kind=2, fma_iters=10**8 + 1) == bd.EINVAL
     assert "scratch" in bd.strerror(bd.ETOOLARGE)
+
+
+# Invalid probe configurations: both probe entry points must return the same
+# status for each (they share their field checks; only the burst target differs).
+BAD_PROBE_FIELDS = [
+    dict(K=0), dict(K=1025), dict(rounds=0), dict(V_bytes=0), dict(V_bytes=4096 * 4 + 16),
+    dict(G_ns=-1), dict(store_kind=-1), dict(store_kind=2), dict(gap_kind=-1), dict(gap_kind=3),
+    dict(gap_kind=1, fma_iters=-1), dict(gap_kind=1, fma_iters=10**8 + 1),
+    dict(gap_kind=2, fma_iters=-1), dict(gap_kind=2, fma_iters=10**8 + 1),
+    dict(stamps=0), dict(stamps=FAKE + 4),
+]
+
+
+@pytest.mark.parametrize("bad", BAD_PROBE_FIELDS, ids=lambda d: ",".join(f"{k}={v}" for k, v in d.items()))
+def test_probe_entry_points_validate_alike(lib, bad):
+    c = dict(K=4, rounds=3, V_bytes=4096 * 4, G_ns=0, store_kind=0, gap_kind=0, stamps=FAKE, fma_iters=0)
+    c.update(bad)
+
+    def cfg(dst, dst_bytes):
+        return bd.ProbeCfg(c["K"], c["rounds"], c["V_bytes"], c["G_ns"], c["store_kind"], c["gap_kind"],
+                           dst, dst_bytes, c["stamps"], c["fma_iters"])
+
+    rc_run = lib.xstage_probe_run(ctypes.byref(cfg(FAKE, 4096 * 64)), None)
+    rc_noalloc = lib.xstage_probe_run_noalloc(ctypes.byref(cfg(None, 0)), None)
+    assert rc_run == bd.EINVAL
+    assert rc_noalloc == rc_run
 
 
 def test_s2s_validation(lib):

@@ -36,22 +36,31 @@ def summary(stamps, K, rounds):
     return s, t_iss, period
 
 
-@pytest.mark.parametrize("kind", [0, 1])
-def test_noalloc_probe_matches_caller_buffer_probe(kind):
+# (store kind, gap kind, gap iterations): idle gaps with both store kinds, a
+# dependent-FMA gap, and tensor-core work as the gap (needs the larger dynamic
+# shared memory and TMEM).
+CASES = [(0, 0, 0), (1, 0, 0), (0, 1, 4000), (1, 2, 200)]
+
+
+@pytest.mark.parametrize("kind,gap_kind,iters", CASES, ids=lambda x: str(x))
+def test_noalloc_probe_matches_caller_buffer_probe(kind, gap_kind, iters):
     K = bd.num_sms()
     rounds, G_ns = 32, 10_000
     V = (8 * 2**20 // (4096 * K)) * 4096 * K
     target = torch.empty(bd.NOALLOC_MAX_BYTES, dtype=torch.uint8, device="cuda")
     ref_st = torch.zeros(K * rounds * 3, dtype=torch.int64, device="cuda")
-    bd.xstage_probe_run(K, rounds, V, G_ns, target, ref_st, store_kind=kind)
+    bd.xstage_probe_run(K, rounds, V, G_ns, target, ref_st, store_kind=kind, gap_kind=gap_kind, fma_iters=iters)
     torch.cuda.synchronize()
     _, ref_iss, ref_period = summary(ref_st, K, rounds)
     for call in range(2):  # two calls in a row share the library's array
         st = torch.zeros(K * rounds * 3, dtype=torch.int64, device="cuda")
-        bd.xstage_probe_run_noalloc(K, rounds, V, G_ns, st, store_kind=kind)
+        bd.xstage_probe_run_noalloc(K, rounds, V, G_ns, st, store_kind=kind, gap_kind=gap_kind, fma_iters=iters)
         torch.cuda.synchronize()
         s, t_iss, period = summary(st, K, rounds)
-        assert torch.all(s[:, :, 2] - s[:, :, 1] >= G_ns), f"call {call}: gap not honoured"
+        if gap_kind == 0:
+            assert torch.all(s[:, :, 2] - s[:, :, 1] >= G_ns), f"call {call}: gap not honoured"
+        else:
+            assert torch.all(s[:, :, 2] >= s[:, :, 1]), f"call {call}: gap stamps out of order"
         assert abs(t_iss - ref_iss) <= REL_TOL * ref_iss, f"call {call}: issue time {t_iss} vs {ref_iss} ns"
         assert abs(period - ref_period) <= REL_TOL * ref_period, f"call {call}: period {period} vs {ref_period} ns"
 

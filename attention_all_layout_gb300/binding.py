@@ -53,7 +53,7 @@ class Opts(ctypes.Structure):
         ("timeout_ns", ctypes.c_longlong),
         ("inject_stall", ctypes.c_int),
         ("tile_order", ctypes.c_int),
-        ("reserved", ctypes.c_int * 2),
+        ("trace", ctypes.c_void_p),
     ]
 
 
@@ -182,8 +182,26 @@ def _ptr_array(tensors: Sequence[Optional[torch.Tensor]]):
     return arr
 
 
-def _opts(store_kind=0, grid=0, timeout_ns=0, inject_stall=0, tile_order=0) -> Opts:
-    return Opts(store_kind, grid, timeout_ns, inject_stall, tile_order, (ctypes.c_int * 2)(0, 0))
+def _opts(store_kind=0, grid=0, timeout_ns=0, inject_stall=0, tile_order=0, trace=None) -> Opts:
+    return Opts(store_kind, grid, timeout_ns, inject_stall, tile_order, _ptr(trace))
+
+
+TRACE_RECORD = 8  # int64 per (work item, query tile, warp) of a traced call
+
+
+def trace_numel(B: int, H: int, S: int) -> int:
+    """int64 elements of the trace buffer of a traced call (the header's ATTN_A2A_TRACE_BYTES / 8)."""
+    pairs = ((S + 127) // 128 + 1) // 2
+    return B * H * pairs * 2 * 4 * TRACE_RECORD
+
+
+def _check_trace(trace, shp) -> None:
+    if trace is None:
+        return
+    if trace.dtype != torch.int64 or not trace.is_cuda or not trace.is_contiguous():
+        raise ValueError("trace must be a contiguous int64 CUDA tensor")
+    if trace.numel() < trace_numel(shp.B, shp.H, shp.S):
+        raise ValueError(f"trace needs {trace_numel(shp.B, shp.H, shp.S)} int64 elements")
 
 
 def _check(code: int, what: str, check: bool) -> int:
@@ -195,23 +213,26 @@ def _check(code: int, what: str, check: bool) -> int:
 # ------------------------------------------------------------------ entry points (same names as the C ABI)
 def attn_a2a_fwd(q, k, v, P: int, scale: float, out_partitions, dev_status=None, stream=None,
                  store_kind: int = 0, grid: int = 0, timeout_ns: int = 0, inject_stall: int = 0,
-                 tile_order: int = 0, check: bool = True) -> int:
-    """Fused attention + head->sequence all-to-all into `out_partitions` (P tensors [B,c_j,H,d])."""
+                 tile_order: int = 0, trace=None, check: bool = True) -> int:
+    """Fused attention + head->sequence all-to-all into `out_partitions` (P tensors [B,c_j,H,d]).
+    trace: optional device int64 tensor of trace_numel(B, H, S) elements for per-tile stamps."""
     lib = load()
     shp = shape_of(q, k, v)
     parts = _ptr_array(out_partitions)
-    opts = _opts(store_kind, grid, timeout_ns, inject_stall, tile_order)
+    _check_trace(trace, shp)
+    opts = _opts(store_kind, grid, timeout_ns, inject_stall, tile_order, trace)
     rc = lib.attn_a2a_fwd_ex(_ptr(q), _ptr(k), _ptr(v), ctypes.byref(shp), int(P), float(scale), parts,
                              _ptr(dev_status), ctypes.byref(opts), _stream(stream))
     return _check(rc, "attn_a2a_fwd", check)
 
 
 def attn_a2a_fwd_contig(q, k, v, scale: float, out, dev_status=None, stream=None, store_kind: int = 0,
-                        grid: int = 0, timeout_ns: int = 0, check: bool = True) -> int:
+                        grid: int = 0, timeout_ns: int = 0, trace=None, check: bool = True) -> int:
     """The same kernel with a contiguous [B, H, S, d] output ("attention alone")."""
     lib = load()
     shp = shape_of(q, k, v)
-    opts = _opts(store_kind, grid, timeout_ns, 0)
+    _check_trace(trace, shp)
+    opts = _opts(store_kind, grid, timeout_ns, 0, 0, trace)
     rc = lib.attn_a2a_fwd_contig_ex(_ptr(q), _ptr(k), _ptr(v), ctypes.byref(shp), float(scale), _ptr(out),
                                     _ptr(dev_status), ctypes.byref(opts), _stream(stream))
     return _check(rc, "attn_a2a_fwd_contig", check)

@@ -170,7 +170,8 @@ int fwd_common(const void* q, const void* k, const void* v, const attn_a2a_shape
   if (rc != ATTN_A2A_OK) return rc;
   if (opts != nullptr && (opts->store_kind < 0 || opts->store_kind > 2 || opts->grid < 0 ||
                           opts->timeout_ns < 0 || opts->inject_stall < 0 || opts->inject_stall > 1 ||
-                          opts->tile_order < 0 || opts->tile_order > 1))
+                          opts->tile_order < 0 || opts->tile_order > 1 ||
+                          (reinterpret_cast<uintptr_t>(opts->trace) & 7u) != 0))
     return ATTN_A2A_EINVAL;
   // the bulk-store epilogue exists for the contiguous layout and for the
   // all-to-all layout with up to 8 partitions

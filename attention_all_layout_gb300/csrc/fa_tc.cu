@@ -8,7 +8,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "fa_tc.cuh"
+#include "fa_tc_launch.cuh"
 #include "internal.h"
 
 namespace attn_a2a {
@@ -94,22 +94,6 @@ bool make_out_map(CUtensorMap* m, void* base, int B, int H, int H_row, int c, in
   return r == CUDA_SUCCESS;
 }
 
-template <int D, int MODE, int NMAP>
-int launch_t(const tc::Maps<NMAP>& maps, const tc::Params& p, int grid, cudaStream_t stream) {
-  auto kern = tc::fa_fwd_tc_kernel<D, MODE, NMAP>;
-  constexpr int smem = tc::kBulkStores<MODE> ? tc::Cfg<D>::SMEM_ALLOC_STG : tc::Cfg<D>::SMEM_ALLOC;
-  // The in-kernel register split assumes exactly this launch register count;
-  // with fewer registers at launch the softmax warpgroups could never obtain
-  // their share, so refuse to launch rather than risk a stuck kernel.
-  cudaFuncAttributes attr;
-  if (cudaFuncGetAttributes(&attr, kern) != cudaSuccess) return ATTN_A2A_ECUDA;
-  if (attr.numRegs != tc::kLaunchRegs) return ATTN_A2A_EUNSUPPORTED;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-    return ATTN_A2A_ECUDA;
-  kern<<<grid, tc::kThreads, smem, stream>>>(maps, p);
-  return cudaGetLastError() == cudaSuccess ? ATTN_A2A_OK : ATTN_A2A_ECUDA;
-}
-
 void common_params(tc::Params& p, const attn_a2a_shape& shp, float scale, int* dev_status,
                    const attn_a2a_opts& opts) {
   p.B = shp.B;
@@ -164,6 +148,11 @@ int launch_fa_tc(const void* q, const void* k, const void* v, const attn_a2a_sha
     p.interleave = epi.cbase / (2 * tc::kBM);
   const int grid = grid_for(p, opts);
   if (grid <= 0) return ATTN_A2A_ECUDA;
+  if (opts.trace != nullptr) {
+    p.trace = opts.trace;
+    const int mode = a2a ? (bulk ? tc::kModeA2AT : tc::kModeA2A) : (bulk ? tc::kModeContigT : tc::kModeContig);
+    return launch_fa_tc_traced(maps, p, shp.d, mode, grid, stream);
+  }
   if (bulk && a2a)
     return shp.d == 128 ? launch_t<128, tc::kModeA2AT, 1>(maps, p, grid, stream)
                         : launch_t<64, tc::kModeA2AT, 1>(maps, p, grid, stream);

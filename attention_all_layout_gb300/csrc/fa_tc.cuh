@@ -170,6 +170,7 @@ struct Params {
   int nb_big, nb_small;  // kModeS2S: 128-row blocks of a longer / shorter chunk
   int interleave;        // > 1: chunk-interleaved item order with this many pairs per chunk
   int seg;               // kModeS2SG(T): rows per TMA box of the sequence-sharded loads (128 or 64)
+  long long* trace;      // traced instantiations only: kTraceRecord int64 per (item, tile, warp)
   EpiParams epi;
 };
 
@@ -483,6 +484,28 @@ __device__ void relay_role(const Params& p, uint32_t sbase, uint32_t bar0, const
   }
 }
 
+// ------------------------------------------------------------------ per-tile trace
+// Traced instantiations (TRACE = true) record, per work item, query tile t and
+// warp w of the tile's warpgroup, kTraceRecord int64 at
+// trace[((item * 2 + t) * 4 + w) * kTraceRecord]:
+//   0 %globaltimer when the tile's first scores are ready (its Q loop starts)
+//   1 %globaltimer when its O accumulator is final (the Q loop ends)
+//   2 %globaltimer when the warp starts issuing the tile's output stores
+//   3 %globaltimer when the warp has issued them and resumes (for the bulk
+//     stores' issuing thread: after the commit and the wait for the staging
+//     tile to be read)
+//   4 SM clock cycles between 2 and 3 (finer than the timer's resolution)
+//   5 %smid, 6 blockIdx.x, 7 the tile's first sequence row
+// This is the per-tile store-span record of the X-Stage pages' validation
+// ("Results": tensor-core timelines and store-span distributions).
+constexpr int kTraceRecord = 8;
+
+__device__ __forceinline__ uint32_t smid_u32() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(r));
+  return r;
+}
+
 // ------------------------------------------------------------------ softmax / epilogue
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -577,7 +600,7 @@ __device__ __forceinline__ bool bulk_store_tile(const Maps<NMAP>* maps, uint32_t
   return true;
 }
 
-template <int D, int MODE, int NMAP>
+template <int D, int MODE, int NMAP, bool TRACE>
 __device__ void softmax_role(const Params& p, int t, uint32_t bar0, uint32_t tmem, const Maps<NMAP>* maps,
                              uint32_t stg, const WaitCtl& w) {
   using C = Cfg<D>;
@@ -594,6 +617,25 @@ __device__ void softmax_role(const Params& p, int t, uint32_t bar0, uint32_t tme
   for (int item = blockIdx.x; item < p.total; item += gridDim.x, ++it) {
     const Item wi = decode_item(p, item);
     const int srow = (2 * wi.pair + t) * kBM + r;
+    uint64_t tr_q0 = 0, tr_q1 = 0, tr_e0 = 0;  // trace stamps (TRACE only)
+    long long tr_c0 = 0;
+    // the warp's record: written by lane 0 once the warp has issued its stores
+    auto trace_out = [&]() {
+      if constexpr (TRACE) {
+        if (lane == 0) {
+          long long* rec = p.trace + ((static_cast<long long>(item) * 2 + t) * 4 + (warp & 3)) * kTraceRecord;
+          const long long c1 = clock64();
+          rec[0] = static_cast<long long>(tr_q0);
+          rec[1] = static_cast<long long>(tr_q1);
+          rec[2] = static_cast<long long>(tr_e0);
+          rec[3] = static_cast<long long>(globaltimer_ns());
+          rec[4] = c1 - tr_c0;
+          rec[5] = smid_u32();
+          rec[6] = blockIdx.x;
+          rec[7] = (2 * wi.pair + t) * kBM;
+        }
+      }
+    };
     float m_used = -INFINITY;
     float l = 0.f;
     BlockWalker<MODE> kb;
@@ -602,6 +644,9 @@ __device__ void softmax_role(const Params& p, int t, uint32_t bar0, uint32_t tme
       const bool got = __all_sync(0xffffffffu, mbar_wait(BAR(C::SF + t), sf_cnt & 1, w));
       if (!got) return;
       ++sf_cnt;
+      if constexpr (TRACE) {
+        if (j == 0) tr_q0 = globaltimer_ns();
+      }
       tc_fence_after();
       uint32_t sr[128];
       tmem_ld_x128(tS, sr);
@@ -653,12 +698,17 @@ __device__ void softmax_role(const Params& p, int t, uint32_t bar0, uint32_t tme
     // ---- epilogue: the tile owner stores its rows to their destination and moves on
     const bool got = __all_sync(0xffffffffu, mbar_wait(BAR(C::OF + t), it & 1, w));
     if (!got) return;
+    if constexpr (TRACE) tr_q1 = globaltimer_ns();
     tc_fence_after();
     uint32_t o[D];
     if constexpr (D == 128) tmem_ld_x128(tO, o);
     else tmem_ld_x64(tO, o);
     tc_fence_before();
     mbar_arrive(BAR(C::OE + t));  // O_t may now be overwritten by the next item
+    if constexpr (TRACE) {
+      tr_e0 = globaltimer_ns();
+      tr_c0 = clock64();
+    }
     if constexpr (kBulkStores<MODE>) {
       // Epilogue uses are numbered u = 2 it + t; use u waits until use u - 1
       // has released the staging buffer (token STG, one phase per use).
@@ -685,6 +735,7 @@ __device__ void softmax_role(const Params& p, int t, uint32_t bar0, uint32_t tme
                                       u > 0, r, lane, elected, o, 1.0f / l, map, y, z, wi.b, w))
           return;
         ++stgw_cnt;
+        trace_out();
         continue;
       }
       // no bulk store for this tile: pass the buffer on in turn
@@ -733,11 +784,12 @@ __device__ void softmax_role(const Params& p, int t, uint32_t bar0, uint32_t tme
         d4[c] = v;
       }
     }
+    trace_out();
   }
 }
 
 // ------------------------------------------------------------------ kernel
-template <int D, int MODE, int NMAP>
+template <int D, int MODE, int NMAP, bool TRACE = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_tc_kernel(const __grid_constant__ Maps<NMAP> maps, const __grid_constant__ Params p) {
   using C = Cfg<D>;
@@ -805,7 +857,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
-    softmax_role<D, MODE, NMAP>(p, (warp - 4) / 4, bar0, tmem, &maps, sbase + C::STG_OFF, w);
+    softmax_role<D, MODE, NMAP, TRACE>(p, (warp - 4) / 4, bar0, tmem, &maps, sbase + C::STG_OFF, w);
     // the bulk-store issuers: every store must have completed before the CTA exits
     if (kBulkStores<MODE> && (warp & 3) == 0 && lane == 0) bulk_wait_all();
   }

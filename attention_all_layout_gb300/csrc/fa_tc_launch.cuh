@@ -1,0 +1,33 @@
+// Launch of one instantiation of the tcgen05 fused attention kernel, shared
+// by the translation unit of the plain kernels and that of the traced ones.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "attn_a2a.h"
+#include "fa_tc.cuh"
+
+namespace attn_a2a {
+
+template <int D, int MODE, int NMAP, bool TRACE = false>
+int launch_t(const tc::Maps<NMAP>& maps, const tc::Params& p, int grid, cudaStream_t stream) {
+  auto kern = tc::fa_fwd_tc_kernel<D, MODE, NMAP, TRACE>;
+  constexpr int smem = tc::kBulkStores<MODE> ? tc::Cfg<D>::SMEM_ALLOC_STG : tc::Cfg<D>::SMEM_ALLOC;
+  // The in-kernel register split assumes exactly this launch register count;
+  // with fewer registers at launch the softmax warpgroups could never obtain
+  // their share, so refuse to launch rather than risk a stuck kernel.
+  cudaFuncAttributes attr;
+  if (cudaFuncGetAttributes(&attr, kern) != cudaSuccess) return ATTN_A2A_ECUDA;
+  if (attr.numRegs != tc::kLaunchRegs) return ATTN_A2A_EUNSUPPORTED;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return ATTN_A2A_ECUDA;
+  kern<<<grid, tc::kThreads, smem, stream>>>(maps, p);
+  return cudaGetLastError() == cudaSuccess ? ATTN_A2A_OK : ATTN_A2A_ECUDA;
+}
+
+// The traced instantiations (per-tile stamps into p.trace) of the four
+// head-sharded modes: kModeContig, kModeA2A, kModeA2AT, kModeContigT.
+int launch_fa_tc_traced(const tc::Maps<1>& maps, const tc::Params& p, int d, int mode, int grid,
+                        cudaStream_t stream);
+
+}  // namespace attn_a2a

@@ -100,8 +100,30 @@ typedef struct {
                            items cycle through the P destination partitions, spreading
                            each wave's store burst over all of them (burst shaping).
                            Results are identical; only the store pattern changes */
-  int reserved[2];
+  long long* trace;     /* NULL in normal use. Device int64 buffer of at least
+                           ATTN_A2A_TRACE_BYTES(B, H, S) bytes, 8-byte aligned: runs
+                           the traced instantiation of the same kernel, which records
+                           per work item, query tile t and warp w of the tile owner
+                           ATTN_A2A_TRACE_RECORD int64 at
+                           trace[((item*2 + t)*4 + w) * ATTN_A2A_TRACE_RECORD]:
+                           [0] %globaltimer ns when the tile's first scores are ready,
+                           [1] when its output accumulator is final, [2] when the warp
+                           starts issuing the tile's stores, [3] when it has issued them
+                           and resumes; [4] SM cycles from [2] to [3]; [5] SM id;
+                           [6] CTA index; [7] the tile's first sequence row. A work item
+                           is a pair of 128-row query tiles of one (b, h):
+                           item = (b*H + h) * ceil(ceil(S/128)/2) + pair, and CTA c runs
+                           items c, c + grid, ... (the X-Stage pages' "Results":
+                           per-tile store spans and tensor-core timelines). Results are
+                           identical to the untraced call. attn_a2a_fwd_ex and
+                           attn_a2a_fwd_contig_ex only */
 } attn_a2a_opts;
+
+/* Trace record of attn_a2a_opts.trace: int64 per (work item, tile, warp), and
+ * the buffer size in bytes for B, H, S. */
+#define ATTN_A2A_TRACE_RECORD 8
+#define ATTN_A2A_TRACE_BYTES(B, H, S) \
+  ((long long)(B) * (H) * ((((long long)(S) + 127) / 128 + 1) / 2) * 2 * 4 * ATTN_A2A_TRACE_RECORD * 8)
 
 /*
  * attn_a2a_fwd - fused attention + head-to-sequence all-to-all (the product).

@@ -54,6 +54,8 @@ class Opts(ctypes.Structure):
         ("inject_stall", ctypes.c_int),
         ("tile_order", ctypes.c_int),
         ("trace", ctypes.c_void_p),
+        ("part_heads", ctypes.c_int),
+        ("reserved", ctypes.c_int),
     ]
 
 
@@ -175,15 +177,20 @@ def alloc_partitions(B: int, S: int, H: int, d: int, P: int, device="cuda", fill
     return parts
 
 
-def _ptr_array(tensors: Sequence[Optional[torch.Tensor]]):
+def _ptr_array(tensors: Sequence):
+    """Host array of device pointers: tensors (empty ones as NULL), raw integer
+    addresses (e.g. offsets into partitions shared by several head groups), or None."""
     arr = (ctypes.c_void_p * max(1, len(tensors)))()
     for i, t in enumerate(tensors):
-        arr[i] = None if (t is None or t.numel() == 0) else t.data_ptr()
+        if isinstance(t, int):
+            arr[i] = t or None
+        else:
+            arr[i] = None if (t is None or t.numel() == 0) else t.data_ptr()
     return arr
 
 
-def _opts(store_kind=0, grid=0, timeout_ns=0, inject_stall=0, tile_order=0, trace=None) -> Opts:
-    return Opts(store_kind, grid, timeout_ns, inject_stall, tile_order, _ptr(trace))
+def _opts(store_kind=0, grid=0, timeout_ns=0, inject_stall=0, tile_order=0, trace=None, part_heads=0) -> Opts:
+    return Opts(store_kind, grid, timeout_ns, inject_stall, tile_order, _ptr(trace), part_heads, 0)
 
 
 TRACE_RECORD = 8  # int64 per (work item, query tile, warp) of a traced call
@@ -213,14 +220,16 @@ def _check(code: int, what: str, check: bool) -> int:
 # ------------------------------------------------------------------ entry points (same names as the C ABI)
 def attn_a2a_fwd(q, k, v, P: int, scale: float, out_partitions, dev_status=None, stream=None,
                  store_kind: int = 0, grid: int = 0, timeout_ns: int = 0, inject_stall: int = 0,
-                 tile_order: int = 0, trace=None, check: bool = True) -> int:
+                 tile_order: int = 0, trace=None, part_heads: int = 0, check: bool = True) -> int:
     """Fused attention + head->sequence all-to-all into `out_partitions` (P tensors [B,c_j,H,d]).
-    trace: optional device int64 tensor of trace_numel(B, H, S) elements for per-tile stamps."""
+    trace: optional device int64 tensor of trace_numel(B, H, S) elements for per-tile stamps.
+    part_heads: heads per partition row for a head-group launch (0 = H); the partitions are then
+    given as device addresses already offset to the group's first head (see ulysses.py)."""
     lib = load()
     shp = shape_of(q, k, v)
     parts = _ptr_array(out_partitions)
     _check_trace(trace, shp)
-    opts = _opts(store_kind, grid, timeout_ns, inject_stall, tile_order, trace)
+    opts = _opts(store_kind, grid, timeout_ns, inject_stall, tile_order, trace, part_heads)
     rc = lib.attn_a2a_fwd_ex(_ptr(q), _ptr(k), _ptr(v), ctypes.byref(shp), int(P), float(scale), parts,
                              _ptr(dev_status), ctypes.byref(opts), _stream(stream))
     return _check(rc, "attn_a2a_fwd", check)

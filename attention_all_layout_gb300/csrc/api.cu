@@ -69,9 +69,14 @@ int check_inputs(const void* q, const void* k, const void* v, const attn_a2a_sha
 
 // Partition pointers and the chunk rule: chunk j has floor(S/P) rows plus one
 // for j < S mod P (torch.tensor_split).
-int make_partitions(const attn_a2a_shape& shp, int P, void* const* parts, EpiParams* e) {
+// part_heads = heads per partition row (0 = H): a launch over one head group
+// writes heads [0, H) of rows that hold part_heads heads (the caller offsets
+// each partition pointer to the group's first head); the head-sharding rule
+// then applies to the full row.
+int make_partitions(const attn_a2a_shape& shp, int P, void* const* parts, EpiParams* e, int part_heads = 0) {
   if (P < 1 || P > kMaxRanks) return ATTN_A2A_EINVAL;
-  if (shp.H % P != 0) return ATTN_A2A_EINVAL;
+  const int h_row = part_heads > 0 ? part_heads : shp.H;
+  if (h_row < shp.H || h_row % P != 0) return ATTN_A2A_EINVAL;
   if (parts == nullptr) return ATTN_A2A_EINVAL;
   std::memset(e, 0, sizeof(*e));
   e->P = P;
@@ -83,6 +88,7 @@ int make_partitions(const attn_a2a_shape& shp, int P, void* const* parts, EpiPar
     if (has_bytes && (parts[j] == nullptr || !aligned16(parts[j]))) return ATTN_A2A_EINVAL;
     e->part[j] = parts[j];
   }
+  e->hstride = part_heads > 0 ? part_heads : 0;
   return ATTN_A2A_OK;
 }
 
@@ -91,7 +97,10 @@ bool partitions_alias_inputs(const attn_a2a_shape& shp, const EpiParams& e, cons
     const int c = e.cbase + (j < e.crem ? 1 : 0);
     if (c == 0) continue;
     const uintptr_t lo = reinterpret_cast<uintptr_t>(e.part[j]);
-    const Span out{lo, lo + static_cast<uintptr_t>(shp.B) * c * shp.H * shp.d * 2u};
+    // rows of h_row heads, of which this call writes the first H
+    const long long h_row = e.hstride > 0 ? e.hstride : shp.H;
+    const long long last = (static_cast<long long>(shp.B) * c - 1) * h_row + shp.H;
+    const Span out{lo, lo + static_cast<uintptr_t>(last) * shp.d * 2u};
     for (int i = 0; i < nin; ++i)
       if (overlaps(out, in[i])) return true;
   }
@@ -171,7 +180,8 @@ int fwd_common(const void* q, const void* k, const void* v, const attn_a2a_shape
   if (opts != nullptr && (opts->store_kind < 0 || opts->store_kind > 2 || opts->grid < 0 ||
                           opts->timeout_ns < 0 || opts->inject_stall < 0 || opts->inject_stall > 1 ||
                           opts->tile_order < 0 || opts->tile_order > 1 ||
-                          (reinterpret_cast<uintptr_t>(opts->trace) & 7u) != 0))
+                          (reinterpret_cast<uintptr_t>(opts->trace) & 7u) != 0 || opts->part_heads < 0 ||
+                          (opts->part_heads > 0 && !a2a)))
     return ATTN_A2A_EINVAL;
   // the bulk-store epilogue exists for the contiguous layout and for the
   // all-to-all layout with up to 8 partitions
@@ -179,7 +189,7 @@ int fwd_common(const void* q, const void* k, const void* v, const attn_a2a_shape
   EpiParams epi;
   std::memset(&epi, 0, sizeof(epi));
   if (a2a) {
-    rc = make_partitions(*shp, P, out_partitions, &epi);
+    rc = make_partitions(*shp, P, out_partitions, &epi, opts != nullptr ? opts->part_heads : 0);
     if (rc != ATTN_A2A_OK) return rc;
   } else {
     epi.P = 1;

@@ -117,13 +117,22 @@ typedef struct {
                            per-tile store spans and tensor-core timelines). Results are
                            identical to the untraced call. attn_a2a_fwd_ex and
                            attn_a2a_fwd_contig_ex only */
+  int part_heads;       /* 0 in normal use (= H). Ulysses head-group launch, all-to-all
+                           layout only: the heads per row of each output partition,
+                           >= H and a multiple of P. The call computes its H heads (one
+                           rank's head group, e.g. heads [r*part_heads/P, (r+1)*part_heads/P)
+                           of the layer) and stores head h of sequence row s at
+                           out_partitions[j][(b*c_j + s - start_j)*part_heads + h] * d,
+                           so the caller passes each partition pointer already offset
+                           to the group's first head (h0 * d elements). P such calls,
+                           one per head group, fill the partitions exactly as one call
+                           over all part_heads heads does, byte for byte. Where the
+                           partitions are another GPU's memory mapped into this one's
+                           address space, this is the one-sided store of the pages'
+                           FlashAttention-A2A ("Key Contributions") from rank r's tile
+                           owners into rank j's buffer */
+  int reserved;
 } attn_a2a_opts;
-
-/* Trace record of attn_a2a_opts.trace: int64 per (work item, tile, warp), and
- * the buffer size in bytes for B, H, S. */
-#define ATTN_A2A_TRACE_RECORD 8
-#define ATTN_A2A_TRACE_BYTES(B, H, S) \
-  ((long long)(B) * (H) * ((((long long)(S) + 127) / 128 + 1) / 2) * 2 * 4 * ATTN_A2A_TRACE_RECORD * 8)
 
 /*
  * attn_a2a_fwd - fused attention + head-to-sequence all-to-all (the product).
@@ -133,7 +142,8 @@ typedef struct {
  * split row by row; rows >= S are never stored.
  *   q, k, v        : device bf16, layout above, caller-owned, read only.
  *   shp            : host pointer to the shape/strides.
- *   P              : virtual ranks, 1 <= P <= 64, H % P == 0.
+ *   P              : virtual ranks, 1 <= P <= 64, H % P == 0 (with
+ *                    attn_a2a_opts.part_heads: part_heads % P == 0 instead).
  *   scale          : softmax scale, finite and >= 0 (1/sqrt(d) in DiT).
  *   out_partitions : HOST array of P device pointers, partition j is
  *                    [B, c_j, H, d] bf16 contiguous (may be NULL if c_j == 0).

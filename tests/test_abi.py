@@ -236,3 +236,21 @@ def test_moe_validation(lib):
     assert run(P=0) == bd.EINVAL
     assert run(n_tasks=-1) == bd.EINVAL
     assert run(n_tasks=0) == bd.OK  # nothing to do, nothing launched
+
+
+def test_part_heads_validation(lib):
+    def run(H=4, P=2, part_heads=0, a2a=True):
+        opts = bd._opts(part_heads=part_heads)
+        shp = bd.plain_shape(1, H, 256, 64)
+        parts = (ctypes.c_void_p * P)(*[FAKE * (16 + j) for j in range(P)])
+        if a2a:
+            return lib.attn_a2a_fwd_ex(FAKE, FAKE * 2, FAKE * 3, ctypes.byref(shp), P, 0.125, parts, None,
+                                       ctypes.byref(opts), None)
+        return lib.attn_a2a_fwd_contig_ex(FAKE, FAKE * 2, FAKE * 3, ctypes.byref(shp), 0.125, FAKE * 16, None,
+                                          ctypes.byref(opts), None)
+
+    assert run(H=4, part_heads=2) == bd.EINVAL          # fewer heads per row than the call computes
+    assert run(H=2, P=4, part_heads=6) == bd.EINVAL     # a row of 6 heads does not split over 4 ranks
+    assert run(H=1, P=4, part_heads=4, a2a=False) == bd.EINVAL  # contiguous layout has no partitions
+    assert run(part_heads=-1) == bd.EINVAL
+

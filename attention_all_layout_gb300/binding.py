@@ -56,6 +56,8 @@ class Opts(ctypes.Structure):
         ("trace", ctypes.c_void_p),
         ("part_heads", ctypes.c_int),
         ("reserved", ctypes.c_int),
+        ("workspace", ctypes.c_void_p),
+        ("workspace_bytes", ctypes.c_longlong),
     ]
 
 
@@ -189,8 +191,24 @@ def _ptr_array(tensors: Sequence):
     return arr
 
 
-def _opts(store_kind=0, grid=0, timeout_ns=0, inject_stall=0, tile_order=0, trace=None, part_heads=0) -> Opts:
-    return Opts(store_kind, grid, timeout_ns, inject_stall, tile_order, _ptr(trace), part_heads, 0)
+def _opts(store_kind=0, grid=0, timeout_ns=0, inject_stall=0, tile_order=0, trace=None, part_heads=0,
+          workspace=None) -> Opts:
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    return Opts(store_kind, grid, timeout_ns, inject_stall, tile_order, _ptr(trace), part_heads, 0,
+                _ptr(workspace), ws_bytes)
+
+
+def workspace_bytes(grid: int, d: int) -> int:
+    """Bytes of the split-tail workspace for `grid` CTAs and head dim d (the header's
+    ATTN_A2A_WORKSPACE_BYTES)."""
+    return 256 + 32 * grid + 1024 * grid * (d + 2)
+
+
+def alloc_workspace(d: int = 128, grid: int = 0, device="cuda") -> torch.Tensor:
+    """A zeroed split-tail workspace (attn_a2a_opts.workspace) for up to `grid` CTAs
+    (0 = one per SM). Reusable by every later call on the same stream."""
+    g = grid or num_sms()
+    return torch.zeros(workspace_bytes(g, d), dtype=torch.uint8, device=device)
 
 
 TRACE_RECORD = 8  # int64 per (work item, query tile, warp) of a traced call
@@ -220,28 +238,30 @@ def _check(code: int, what: str, check: bool) -> int:
 # ------------------------------------------------------------------ entry points (same names as the C ABI)
 def attn_a2a_fwd(q, k, v, P: int, scale: float, out_partitions, dev_status=None, stream=None,
                  store_kind: int = 0, grid: int = 0, timeout_ns: int = 0, inject_stall: int = 0,
-                 tile_order: int = 0, trace=None, part_heads: int = 0, check: bool = True) -> int:
+                 tile_order: int = 0, trace=None, part_heads: int = 0, workspace=None, check: bool = True) -> int:
     """Fused attention + head->sequence all-to-all into `out_partitions` (P tensors [B,c_j,H,d]).
     trace: optional device int64 tensor of trace_numel(B, H, S) elements for per-tile stamps.
     part_heads: heads per partition row for a head-group launch (0 = H); the partitions are then
-    given as device addresses already offset to the group's first head (see ulysses.py)."""
+    given as device addresses already offset to the group's first head (see ulysses.py).
+    workspace: optional zeroed uint8 tensor (alloc_workspace) that lets a partial last wave of
+    work items be split over all CTAs."""
     lib = load()
     shp = shape_of(q, k, v)
     parts = _ptr_array(out_partitions)
     _check_trace(trace, shp)
-    opts = _opts(store_kind, grid, timeout_ns, inject_stall, tile_order, trace, part_heads)
+    opts = _opts(store_kind, grid, timeout_ns, inject_stall, tile_order, trace, part_heads, workspace)
     rc = lib.attn_a2a_fwd_ex(_ptr(q), _ptr(k), _ptr(v), ctypes.byref(shp), int(P), float(scale), parts,
                              _ptr(dev_status), ctypes.byref(opts), _stream(stream))
     return _check(rc, "attn_a2a_fwd", check)
 
 
 def attn_a2a_fwd_contig(q, k, v, scale: float, out, dev_status=None, stream=None, store_kind: int = 0,
-                        grid: int = 0, timeout_ns: int = 0, trace=None, check: bool = True) -> int:
+                        grid: int = 0, timeout_ns: int = 0, trace=None, workspace=None, check: bool = True) -> int:
     """The same kernel with a contiguous [B, H, S, d] output ("attention alone")."""
     lib = load()
     shp = shape_of(q, k, v)
     _check_trace(trace, shp)
-    opts = _opts(store_kind, grid, timeout_ns, 0, 0, trace)
+    opts = _opts(store_kind, grid, timeout_ns, 0, 0, trace, 0, workspace)
     rc = lib.attn_a2a_fwd_contig_ex(_ptr(q), _ptr(k), _ptr(v), ctypes.byref(shp), float(scale), _ptr(out),
                                     _ptr(dev_status), ctypes.byref(opts), _stream(stream))
     return _check(rc, "attn_a2a_fwd_contig", check)

@@ -210,6 +210,28 @@ int fwd_common(const void* q, const void* k, const void* v, const attn_a2a_shape
     for (const Span& s : in)
       if (overlaps(out, s)) return ATTN_A2A_EINVAL;
   }
+  if (opts != nullptr && opts->workspace != nullptr) {
+    // split-tail scratch: aligned, and apart from every input and output
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(opts->workspace);
+    if ((lo & 255u) != 0 || opts->workspace_bytes <= 0) return ATTN_A2A_EINVAL;
+    const Span ws{lo, lo + static_cast<uintptr_t>(opts->workspace_bytes)};
+    for (const Span& s : in)
+      if (overlaps(ws, s)) return ATTN_A2A_EINVAL;
+    if (a2a) {
+      const long long h_row = epi.hstride > 0 ? epi.hstride : shp->H;
+      for (int j = 0; j < epi.P; ++j) {
+        const int c = epi.cbase + (j < epi.crem ? 1 : 0);
+        if (c == 0) continue;
+        const uintptr_t plo = reinterpret_cast<uintptr_t>(epi.part[j]);
+        const long long last = (static_cast<long long>(shp->B) * c - 1) * h_row + shp->H;
+        if (overlaps(ws, Span{plo, plo + static_cast<uintptr_t>(last) * shp->d * 2u})) return ATTN_A2A_EINVAL;
+      }
+    } else {
+      const uintptr_t olo = reinterpret_cast<uintptr_t>(out_contig);
+      if (overlaps(ws, Span{olo, olo + static_cast<uintptr_t>(shp->B) * shp->H * shp->S * shp->d * 2u}))
+        return ATTN_A2A_EINVAL;
+    }
+  }
   const attn_a2a_opts o = opts ? *opts : default_opts();
   return launch_fa_tc(q, k, v, *shp, scale, a2a, epi, dev_status, o, static_cast<cudaStream_t>(stream));
 }

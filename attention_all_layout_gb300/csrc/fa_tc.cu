@@ -4,6 +4,8 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+#include <climits>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -105,6 +107,56 @@ void common_params(tc::Params& p, const attn_a2a_shape& shp, float scale, int* d
   p.inject_stall = opts.inject_stall;
 }
 
+// Launch ids for the split tail's workspace flags: every launch that splits its
+// tail gets a new one (never 0, the value of a zeroed workspace), so flags left
+// by an earlier launch - finished or aborted - never match.
+std::atomic<unsigned> g_epoch{0};
+
+unsigned next_epoch() {
+  unsigned e;
+  do {
+    e = g_epoch.fetch_add(1u, std::memory_order_relaxed) + 1u;
+  } while (e == 0u);
+  return e;
+}
+
+// Fewest key blocks per CTA that a split tail must save over the unsplit last
+// wave (nblk - tail_len) before it is used. A tail piece restarts the
+// two-tile pipeline (Q loads, first block, drain) and a split item pays for
+// its partials' writes and merge: measured on GB300, a tail of 17-block ranges
+// instead of 32-block items (the image preset) ran 42 us without the merge
+// instead of about 30, and the partials' write and merge added about 17 us,
+// so that the split lost 6 % there (joint, 31 of 36 blocks: lost 10 %); at
+// the video and long presets (80 and 62 blocks saved) it gained 0.3-0.8 %.
+constexpr int kSplitMinSavedBlocks = 32;
+
+// Split tail (the kernel's tail_piece): when the last wave holds r < grid
+// items, its r * nblk key blocks are divided into ranges of
+// ceil(r * nblk / grid) <= nblk blocks, one per CTA, if that saves at least
+// kSplitMinSavedBlocks blocks per CTA. Needs the caller's workspace; returns
+// ATTN_A2A_EINVAL if it is too small.
+int plan_split_tail(tc::Params& p, int grid, int d, const attn_a2a_opts& opts) {
+  p.tail_first = p.total;
+  p.tail_len = 0;
+  if (opts.workspace == nullptr) return ATTN_A2A_OK;
+  if (opts.workspace_bytes < ATTN_A2A_WORKSPACE_BYTES(grid, d)) return ATTN_A2A_EINVAL;
+  if (opts.trace != nullptr || p.interleave > 1 || p.nblk < 2 || p.nblk > (1 << 20)) return ATTN_A2A_OK;
+  const int waves = (p.total + grid - 1) / grid;
+  const int r = p.total - (waves - 1) * grid;
+  if (r >= grid) return ATTN_A2A_OK;  // the last wave is full
+  const int len = static_cast<int>((static_cast<long long>(r) * p.nblk + grid - 1) / grid);
+  if (p.nblk - len < kSplitMinSavedBlocks) return ATTN_A2A_OK;
+  p.tail_first = (waves - 1) * grid;
+  p.tail_len = len;
+  uint8_t* base = static_cast<uint8_t*>(opts.workspace);
+  const size_t flags = (static_cast<size_t>(grid) * 32u + 255u) / 256u * 256u;
+  p.ws_flags = reinterpret_cast<unsigned*>(base);
+  p.ws_o = reinterpret_cast<float*>(base + flags);
+  p.ws_ml = p.ws_o + static_cast<size_t>(grid) * 2 * tc::kBM * d;
+  p.epoch = next_epoch();
+  return ATTN_A2A_OK;
+}
+
 int grid_for(const tc::Params& p, const attn_a2a_opts& opts) {
   int grid = opts.grid > 0 ? opts.grid : num_sms_current_device();
   if (grid <= 0) return 0;
@@ -112,6 +164,8 @@ int grid_for(const tc::Params& p, const attn_a2a_opts& opts) {
 }
 
 }  // namespace
+
+int launch_plain(const tc::Maps<1>& maps, const tc::Params& p, int d, int mode, int grid, cudaStream_t stream);
 
 int launch_fa_tc(const void* q, const void* k, const void* v, const attn_a2a_shape& shp,
                  float scale, bool a2a, const EpiParams& epi, int* dev_status,
@@ -148,22 +202,40 @@ int launch_fa_tc(const void* q, const void* k, const void* v, const attn_a2a_sha
     p.interleave = epi.cbase / (2 * tc::kBM);
   const int grid = grid_for(p, opts);
   if (grid <= 0) return ATTN_A2A_ECUDA;
+  const int split_rc = plan_split_tail(p, grid, shp.d, opts);
+  if (split_rc != ATTN_A2A_OK) return split_rc;
+  const int mode = a2a ? (bulk ? tc::kModeA2AT : tc::kModeA2A) : (bulk ? tc::kModeContigT : tc::kModeContig);
   if (opts.trace != nullptr) {
     p.trace = opts.trace;
-    const int mode = a2a ? (bulk ? tc::kModeA2AT : tc::kModeA2A) : (bulk ? tc::kModeContigT : tc::kModeContig);
     return launch_fa_tc_traced(maps, p, shp.d, mode, grid, stream);
   }
-  if (bulk && a2a)
-    return shp.d == 128 ? launch_t<128, tc::kModeA2AT, 1>(maps, p, grid, stream)
-                        : launch_t<64, tc::kModeA2AT, 1>(maps, p, grid, stream);
-  if (bulk)
-    return shp.d == 128 ? launch_t<128, tc::kModeContigT, 1>(maps, p, grid, stream)
-                        : launch_t<64, tc::kModeContigT, 1>(maps, p, grid, stream);
-  if (shp.d == 128)
-    return a2a ? launch_t<128, tc::kModeA2A, 1>(maps, p, grid, stream)
-               : launch_t<128, tc::kModeContig, 1>(maps, p, grid, stream);
-  return a2a ? launch_t<64, tc::kModeA2A, 1>(maps, p, grid, stream)
-             : launch_t<64, tc::kModeContig, 1>(maps, p, grid, stream);
+  if (p.tail_first < p.total) {
+    // the full waves in the plain kernel, then the tail kernel behind it
+    tc::Params pm = p;
+    pm.total = p.tail_first;
+    pm.tail_first = pm.total;
+    const int rc = launch_plain(maps, pm, shp.d, mode, grid, stream);
+    if (rc != ATTN_A2A_OK) return rc;
+    return launch_fa_tc_split(maps, p, shp.d, mode, grid, stream);
+  }
+  return launch_plain(maps, p, shp.d, mode, grid, stream);
+}
+
+int launch_plain(const tc::Maps<1>& maps, const tc::Params& p, int d, int mode, int grid, cudaStream_t stream) {
+  switch (mode) {
+    case tc::kModeA2AT:
+      return d == 128 ? launch_t<128, tc::kModeA2AT, 1>(maps, p, grid, stream)
+                      : launch_t<64, tc::kModeA2AT, 1>(maps, p, grid, stream);
+    case tc::kModeContigT:
+      return d == 128 ? launch_t<128, tc::kModeContigT, 1>(maps, p, grid, stream)
+                      : launch_t<64, tc::kModeContigT, 1>(maps, p, grid, stream);
+    case tc::kModeA2A:
+      return d == 128 ? launch_t<128, tc::kModeA2A, 1>(maps, p, grid, stream)
+                      : launch_t<64, tc::kModeA2A, 1>(maps, p, grid, stream);
+    default:
+      return d == 128 ? launch_t<128, tc::kModeContig, 1>(maps, p, grid, stream)
+                      : launch_t<64, tc::kModeContig, 1>(maps, p, grid, stream);
+  }
 }
 
 int launch_fa_tc_s2s(const void* const* qp, const void* const* kp, const void* const* vp,
@@ -207,6 +279,7 @@ int launch_fa_tc_s2s(const void* const* qp, const void* const* kp, const void* c
     p.npair = (p.nblk + 1) / 2;
     p.total = shp.B * shp.H * p.npair;
     p.epi = epi;
+    p.tail_first = p.total;  // no split tail in the whole-layer modes
     const int grid = grid_for(p, opts);
     if (grid <= 0) return ATTN_A2A_ECUDA;
     if (kind == 1) {
@@ -224,6 +297,7 @@ int launch_fa_tc_s2s(const void* const* qp, const void* const* kp, const void* c
   p.npair = (p.nblk + 1) / 2;
   p.total = shp.B * shp.H * p.npair;
   p.epi = epi;
+  p.tail_first = p.total;  // no split tail in the whole-layer modes
   const int grid = grid_for(p, opts);
   if (grid <= 0) return ATTN_A2A_ECUDA;
   if (shp.d == 128) return launch_t<128, tc::kModeS2S, tc::kMaxS2SRanks>(maps, p, grid, stream);

@@ -63,14 +63,6 @@ constexpr uint32_t kTmemCols = 512;
 // the fp32 accumulators stay far from overflow); past it the block's own
 // maximum is taken and O and l are rescaled.
 constexpr float kSpecBound = 4096.0f;  // 2^12
-// Every kPolyEvery-th pair of probabilities is exponentiated on the FMA pipe
-// (exp2_poly_x2) instead of the MUFU; 0 = all on the MUFU. Off: GB300's MUFU
-// keeps up with the softmax here, and moving 1/8, 1/4 or 1/2 of the pairs to
-// the FMA pipe measured 2 %, 4 % and 9 % slower on the video shape.
-#ifndef ATTN_A2A_POLY_EVERY
-#define ATTN_A2A_POLY_EVERY 0
-#endif
-constexpr int kPolyEvery = ATTN_A2A_POLY_EVERY;
 // Register split (setmaxnreg): the kernel launches with kLaunchRegs per thread;
 // warpgroup 0 (producer, MMA issuer, relay, one idle warp) gives registers back and
 // the two softmax warpgroups take them: 128*kRegsLow + 256*kRegsHigh must not
@@ -171,6 +163,15 @@ struct Params {
   int interleave;        // > 1: chunk-interleaved item order with this many pairs per chunk
   int seg;               // kModeS2SG(T): rows per TMA box of the sequence-sharded loads (128 or 64)
   long long* trace;      // traced instantiations only: kTraceRecord int64 per (item, tile, warp)
+  // Split tail (see tail_pieces): items [tail_first, total) are divided over
+  // the CTAs by key blocks, tail_len blocks per CTA; tail_first = total when
+  // the tail is not split. Partial results go through the caller's workspace.
+  int tail_first, tail_len;
+  unsigned epoch;        // this launch's id, written to the workspace flags
+  float* ws_o;           // [grid][2 tiles][D/4][128 rows] float4: a partial piece's O (unnormalised);
+                         // row-minor, so that a warp's 32 rows are 512 contiguous bytes
+  float* ws_ml;          // [grid][2][128][2] fp32: its running maximum (log2 domain) and row sum
+  unsigned* ws_flags;    // [grid][2][4 warps]: epoch once that warp's rows are written
   EpiParams epi;
 };
 
@@ -253,6 +254,75 @@ struct Item {
   int b, h, pair;
 };
 
+// ------------------------------------------------------------------ split tail
+// The last wave of work items usually holds fewer items than there are CTAs
+// (the image preset: 384 items on 152 CTAs, a last wave of 80). Instead of
+// leaving the other CTAs idle, the tail items' key blocks, counted one item
+// after the other (u = (item - tail_first) * nblk + key block), are divided
+// into equal ranges of tail_len blocks, one per CTA. A CTA's range cuts items
+// into pieces [k0, k1) of their key blocks: a piece that ends inside its item
+// ("partial") writes its unnormalised O, running maximum and row sum to the
+// workspace slot of its CTA and raises a flag; the piece that holds an item's
+// last key block ("final", k0 > 0) waits for the partials of the same item -
+// they belong to the CTAs just before it - merges them into its own and
+// stores the tile as usual. tail_len <= nblk, so a range touches at most two
+// items, and at most one piece per CTA is partial (its range's last). Each CTA
+// runs its partial piece first: final pieces wait only on pieces that never
+// wait, and they are held by lower-numbered CTAs, which start no later.
+// The tail runs as a second kernel (SPLIT = true) right behind the plain one
+// (items below tail_first): the plain kernel lets it launch at once
+// (programmatic dependent launch), so each of its CTAs starts on the SM that
+// a plain CTA leaves. The tail kernel reads only q, k and v, which the plain
+// kernel does not write, so it needs no wait for the plain kernel's results;
+// keeping the tail apart leaves the plain kernel's code and registers as they
+// are.
+struct Piece {
+  int item, k0, k1;
+  int kind;  // 0: a whole item; 1: partial (to the workspace); 2: final piece of a split item
+};
+
+// Tail piece k (0 or 1) of this CTA, in processing order: the range's last
+// piece first when it ends inside its item (a partial that later CTAs' final
+// pieces wait for), then the others in order. False when there is none.
+__device__ __forceinline__ bool tail_piece(const Params& p, int k, Piece& out) {
+  const int R = (p.total - p.tail_first) * p.nblk;
+  const int u0 = static_cast<int>(blockIdx.x) * p.tail_len;
+  const int u1 = min(u0 + p.tail_len, R);
+  if (u0 >= u1) return false;
+  const int i0 = u0 / p.nblk, i1 = (u1 - 1) / p.nblk;
+  const int k0_first = u0 - i0 * p.nblk;
+  const int k1_last = u1 - i1 * p.nblk;
+  if (k1_last < p.nblk) {
+    if (k == 0) {
+      out = Piece{p.tail_first + i1, i1 == i0 ? k0_first : 0, k1_last, 1};
+      return true;
+    }
+    if (i1 == i0) return false;
+    out = Piece{p.tail_first + i0, k0_first, p.nblk, k0_first > 0 ? 2 : 0};  // k == 1: the first item's end
+    return k == 1;
+  }
+  const int i = i0 + k;
+  if (i > i1) return false;
+  const int kb = i == i0 ? k0_first : 0;
+  out = Piece{p.tail_first + i, kb, p.nblk, kb > 0 ? 2 : 0};
+  return true;
+}
+
+// This CTA's piece number `it` (0, 1, ...), a function of it alone, so the
+// roles keep no other loop state; false past the last piece. The plain kernel
+// (SPLIT = false) runs whole items blockIdx.x, blockIdx.x + grid, ... below
+// p.total; the tail kernel (SPLIT = true) runs only this CTA's tail pieces.
+template <bool SPLIT>
+__device__ __forceinline__ bool piece_at(const Params& p, int it, Piece& out) {
+  if constexpr (!SPLIT) {
+    const int item = static_cast<int>(blockIdx.x) + it * static_cast<int>(gridDim.x);
+    out = Piece{item, 0, p.nblk, 0};
+    return item < p.total;
+  } else {
+    return tail_piece(p, it, out);
+  }
+}
+
 __device__ __forceinline__ Item decode_item(const Params& p, int item) {
   Item it;
   it.pair = item % p.npair;
@@ -269,7 +339,7 @@ __device__ __forceinline__ Item decode_item(const Params& p, int item) {
 }
 
 // ------------------------------------------------------------------ producer
-template <int D, int MODE, int NMAP>
+template <int D, int MODE, int NMAP, bool SPLIT>
 __device__ void producer_role(const Params& p, const Maps<NMAP>* maps, uint32_t sbase, uint32_t bar0,
                               const WaitCtl& w) {
   using C = Cfg<D>;
@@ -299,8 +369,9 @@ __device__ void producer_role(const Params& p, const Maps<NMAP>* maps, uint32_t 
         tma_load_4d(piece + a * C::ATOM_BYTES, &tmaps[j], bar, a * 64, l, wi.h, wi.b, pol);
     }
   };
-  for (int item = blockIdx.x; ok && item < p.total; item += gridDim.x, ++it) {
-    const Item wi = decode_item(p, item);
+  for (Piece pc; ok && piece_at<SPLIT>(p, it, pc); ++it) {
+    const int k0 = pc.k0, nb = pc.k1 - pc.k0;
+    const Item wi = decode_item(p, pc.item);
     auto load_q = [&](int t) -> bool {
       if (!mbar_wait(BAR(C::QE + t), (it & 1) ^ 1, w)) return false;
       mbar_arrive_expect_tx(BAR(C::QF + t), C::TILE_BYTES);
@@ -320,6 +391,7 @@ __device__ void producer_role(const Params& p, const Maps<NMAP>* maps, uint32_t 
     };
     BlockWalker<MODE> kw;
     kw.reset(p);
+    if constexpr (MODE != kModeS2S) kw.b = k0;  // (the split tail is not used with per-partition blocks)
     auto load_kv = [&](bool is_v) -> bool {  // the walker's current key block
       const Blk bk = kw.block(p);
       const CUtensorMap* m = is_v ? &maps->v[bk.map] : &maps->k[bk.map];
@@ -340,7 +412,7 @@ __device__ void producer_role(const Params& p, const Maps<NMAP>* maps, uint32_t 
     };
     ok = load_q(0) && load_kv(false) && load_q(1) && load_kv(true);
     kw.next(p);
-    for (int j = 1; ok && j < p.nblk; ++j, kw.next(p)) ok = load_kv(false) && load_kv(true);
+    for (int j = 1; ok && j < nb; ++j, kw.next(p)) ok = load_kv(false) && load_kv(true);
   }
   if (!ok) {
     // Aborting: wait (bounded) for the copies this thread started, so none
@@ -356,7 +428,7 @@ __device__ void producer_role(const Params& p, const Maps<NMAP>* maps, uint32_t 
 }
 
 // ------------------------------------------------------------------ MMA issuer
-template <int D>
+template <int D, bool SPLIT>
 __device__ void mma_role(const Params& p, uint32_t sbase, uint32_t bar0, uint32_t tmem,
                          const WaitCtl& w) {
   using C = Cfg<D>;
@@ -378,8 +450,9 @@ __device__ void mma_role(const Params& p, uint32_t sbase, uint32_t bar0, uint32_
               kIdescQK, kk > 0 ? 1u : 0u);
     }
   };
-  // O_t (+)= P_t V_j; the relay has already seen P_t ready and O_t free.
-  auto issue_pv = [&](int t, int j, uint32_t sV) {
+  // O_t (+)= P_t V_j for key block j (counted from the piece's first) of a
+  // piece of nb blocks; the relay has already seen P_t ready and O_t free.
+  auto issue_pv = [&](int t, int j, uint32_t sV, int nb) {
     const uint32_t vb = sbase + C::KV_OFF + sV * C::TILE_BYTES;
 #pragma unroll
     for (int kk = 0; kk < kBN / 16; ++kk) {
@@ -388,7 +461,7 @@ __device__ void mma_role(const Params& p, uint32_t sbase, uint32_t bar0, uint32_
               (j > 0 || kk > 0) ? 1u : 0u);
     }
     if (t == 1) umma_commit(BAR(C::KVE + sV));  // V_j now read by both tiles
-    if (j == p.nblk - 1) umma_commit(BAR(C::OF + t));
+    if (j == nb - 1) umma_commit(BAR(C::OF + t));
   };
   auto sync = [&]() -> bool {
     if (!counter_wait(cnt_ev, ++ev, w)) return false;
@@ -396,21 +469,24 @@ __device__ void mma_role(const Params& p, uint32_t sbase, uint32_t bar0, uint32_
     return true;
   };
 
-  for (int item = blockIdx.x; ok && item < p.total; item += gridDim.x) {
+  for (int it = 0; ok; ++it) {
+    Piece pc;
+    if (!piece_at<SPLIT>(p, it, pc)) break;
+    const int nb = pc.k1 - pc.k0;
     uint32_t sVprev = 0;
-    if (!sync()) { ok = false; break; }  // A: both Q tiles and K_0
+    if (!sync()) { ok = false; break; }  // A: both Q tiles and the piece's first K
     issue_qk(0, kv_it % C::NSTAGE);
     umma_commit(BAR(C::SF + 0));
-    for (int j = 0; j < p.nblk; ++j) {
+    for (int j = 0; j < nb; ++j) {  // the piece's key blocks, counted from its first
       const uint32_t sK = kv_it % C::NSTAGE;
       if (j > 0) {
         if (!sync()) { ok = false; break; }  // C_j: P1_{j-1} (and O1 free at j = 1)
-        issue_pv(1, j - 1, sVprev);
+        issue_pv(1, j - 1, sVprev, nb);
       }
       issue_qk(1, sK);
       umma_commit(BAR(C::SF + 1));
       umma_commit(BAR(C::KVE + sK));  // K_j read by both tiles
-      if (j == p.nblk - 1) {
+      if (j == nb - 1) {
         umma_commit(BAR(C::QE + 0));
         umma_commit(BAR(C::QE + 1));
       }
@@ -419,16 +495,16 @@ __device__ void mma_role(const Params& p, uint32_t sbase, uint32_t bar0, uint32_
       // B_j: V_j and P0_j (and O0 free at j = 0), and K_{j+1}, so that
       // O0 += P0 V_j and S0_{j+1} go to the tensor core back to back
       if (!sync()) { ok = false; break; }
-      issue_pv(0, j, sV);
+      issue_pv(0, j, sV, nb);
       sVprev = sV;
       ++kv_it;
-      if (j + 1 < p.nblk) {
+      if (j + 1 < nb) {
         issue_qk(0, kv_it % C::NSTAGE);
         umma_commit(BAR(C::SF + 0));
       }
     }
     if (ok && !sync()) ok = false;  // E: P1 of the last block (and O1 free if there is one block)
-    if (ok) issue_pv(1, p.nblk - 1, sVprev);
+    if (ok) issue_pv(1, nb - 1, sVprev, nb);
   }
   if (!ok) {
     // Aborting: let every MMA already issued finish before TMEM is freed.
@@ -448,7 +524,7 @@ __device__ void mma_role(const Params& p, uint32_t sbase, uint32_t bar0, uint32_
 // Each wait depends only on MMAs issued before the event it gates, and the
 // softmax roles cannot run a barrier two phases ahead of these parity waits
 // (their next phase needs an S that is only issued after the relay's event).
-template <int D>
+template <int D, bool SPLIT>
 __device__ void relay_role(const Params& p, uint32_t sbase, uint32_t bar0, const WaitCtl& w) {
   using C = Cfg<D>;
   auto BAR = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
@@ -463,11 +539,12 @@ __device__ void relay_role(const Params& p, uint32_t sbase, uint32_t bar0, const
   };
   auto p_ready = [&](int t) -> bool { return mbar_wait(BAR(C::PF + t), pf_cnt[t]++ & 1, w); };
   auto o_free = [&](int t) -> bool { return mbar_wait(BAR(C::OE + t), (it & 1) ^ 1, w); };
-  for (int item = blockIdx.x; item < p.total; item += gridDim.x, ++it) {
+  for (Piece pc; piece_at<SPLIT>(p, it, pc); ++it) {
+    const int nb = pc.k1 - pc.k0;
     if (!(mbar_wait(BAR(C::QF + 0), it & 1, w) && mbar_wait(BAR(C::QF + 1), it & 1, w))) return;
     if (!kv_ready()) return;
     st_release_u32(cnt_ev, ++ev);  // A
-    for (int j = 0; j < p.nblk; ++j) {
+    for (int j = 0; j < nb; ++j) {
       if (j > 0) {
         if (!p_ready(1)) return;
         if (j == 1 && !o_free(1)) return;
@@ -475,11 +552,11 @@ __device__ void relay_role(const Params& p, uint32_t sbase, uint32_t bar0, const
       }
       if (!kv_ready() || !p_ready(0)) return;  // V_j, P0_j
       if (j == 0 && !o_free(0)) return;
-      if (j + 1 < p.nblk && !kv_ready()) return;  // K_{j+1}
+      if (j + 1 < nb && !kv_ready()) return;  // K_{j+1}
       st_release_u32(cnt_ev, ++ev);  // B_j
     }
     if (!p_ready(1)) return;
-    if (p.nblk == 1 && !o_free(1)) return;
+    if (nb == 1 && !o_free(1)) return;
     st_release_u32(cnt_ev, ++ev);  // E
   }
 }
@@ -544,12 +621,8 @@ __device__ __forceinline__ float probs(const uint32_t (&sr)[128], uint32_t (&pk)
   for (int i = 0; i < 64; ++i) {
     float x0, x1, p0, p1;
     f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1])), scale2, bias2), x0, x1);
-    if (kPolyEvery > 0 && i % (kPolyEvery > 0 ? kPolyEvery : 1) == (kPolyEvery > 0 ? kPolyEvery - 1 : 0)) {
-      exp2_poly_x2(x0, x1, p0, p1);
-    } else {
-      p0 = ex2_approx(x0);
-      p1 = ex2_approx(x1);
-    }
+    p0 = ex2_approx(x0);
+    p1 = ex2_approx(x1);
     if (MASK) {
       p0 = 2 * i < valid ? p0 : 0.f;
       p1 = 2 * i + 1 < valid ? p1 : 0.f;
@@ -600,7 +673,72 @@ __device__ __forceinline__ bool bulk_store_tile(const Maps<NMAP>* maps, uint32_t
   return true;
 }
 
-template <int D, int MODE, int NMAP, bool TRACE>
+// Split tail, partial piece: this thread's row of the tile - unnormalised O
+// (read from TMEM, 32 columns at a time), running maximum m (log2 domain) and
+// row sum l - into the CTA's workspace slot; then the warp's flag is raised to
+// this launch's epoch (every lane's stores fenced first).
+template <int D>
+__device__ __forceinline__ void write_partial(const Params& p, int t, int r, int lane, int w4, uint32_t tO, float m,
+                                              float l) {
+  const size_t tile = static_cast<size_t>(blockIdx.x) * 2 + t;
+  const size_t row = tile * kBM + r;
+  float4* dst = reinterpret_cast<float4*>(p.ws_o) + tile * (D / 4) * kBM + r;  // column group g at dst[g * 128]
+#pragma unroll 1
+  for (int c = 0; c < D / 32; ++c) {
+    uint32_t x[32];
+    tmem_ld_x32(tO + c * 32, x);
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      dst[(c * 8 + i) * kBM] = make_float4(__uint_as_float(x[4 * i]), __uint_as_float(x[4 * i + 1]),
+                                           __uint_as_float(x[4 * i + 2]), __uint_as_float(x[4 * i + 3]));
+  }
+  *reinterpret_cast<float2*>(p.ws_ml + row * 2) = make_float2(m, l);
+  __threadfence();
+  __syncwarp();
+  if (lane == 0) st_release_gpu_u32(p.ws_flags + (blockIdx.x * 2 + t) * 4 + w4, p.epoch);
+}
+
+// Split tail, final piece of `item`: merge the partial pieces of the same item
+// (held by CTAs c_lo .. blockIdx.x - 1, whose ranges cover its first key
+// blocks) into this row's accumulator O in TMEM (tO) and its (m, l): with M
+// the largest maximum, O = sum O_i 2^(m_i - M) and l = sum l_i 2^(m_i - M)
+// over the pieces, the usual combination of softmax partial results. One
+// partial at a time, 32 columns at a time, so that it needs few registers.
+// Each warp waits only for the same warp of the other CTAs (it holds the same
+// rows). Called before O is released to the next piece. False on abort.
+template <int D>
+__device__ __forceinline__ bool merge_partials(const Params& p, int item, int t, int r, int w4, uint32_t tO, float& m,
+                                               float& l, const WaitCtl& w) {
+  const int U = (item - p.tail_first) * p.nblk;
+  for (int cs = U / p.tail_len; cs < static_cast<int>(blockIdx.x); ++cs) {
+    if (!__all_sync(0xffffffffu, flag_wait(p.ws_flags + (cs * 2 + t) * 4 + w4, p.epoch, w))) return false;
+    const size_t tile = static_cast<size_t>(cs) * 2 + t;
+    const size_t row = tile * kBM + r;
+    const float2 ml = *reinterpret_cast<const float2*>(p.ws_ml + row * 2);
+    const float mx = fmaxf(m, ml.x);
+    const float a = ex2_approx(m - mx), b = ex2_approx(ml.x - mx);
+    const float4* src = reinterpret_cast<const float4*>(p.ws_o) + tile * (D / 4) * kBM + r;
+#pragma unroll 1
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t x[32];
+      tmem_ld_x32(tO + c * 32, x);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float4 y = src[(c * 8 + i) * kBM];
+        x[4 * i + 0] = __float_as_uint(fmaf(__uint_as_float(x[4 * i + 0]), a, y.x * b));
+        x[4 * i + 1] = __float_as_uint(fmaf(__uint_as_float(x[4 * i + 1]), a, y.y * b));
+        x[4 * i + 2] = __float_as_uint(fmaf(__uint_as_float(x[4 * i + 2]), a, y.z * b));
+        x[4 * i + 3] = __float_as_uint(fmaf(__uint_as_float(x[4 * i + 3]), a, y.w * b));
+      }
+      tmem_st_x32(tO + c * 32, x);
+    }
+    l = fmaf(l, a, ml.y * b);
+    m = mx;
+  }
+  return true;
+}
+
+template <int D, int MODE, int NMAP, bool TRACE, bool SPLIT>
 __device__ void softmax_role(const Params& p, int t, uint32_t bar0, uint32_t tmem, const Maps<NMAP>* maps,
                              uint32_t stg, const WaitCtl& w) {
   using C = Cfg<D>;
@@ -613,8 +751,14 @@ __device__ void softmax_role(const Params& p, int t, uint32_t bar0, uint32_t tme
   const float sl2 = p.scale_log2;
   uint32_t sf_cnt = 0;
   uint32_t stgw_cnt = 0;  // this tile's bulk stores so far (phases of STGW + t)
-  int it = 0;
-  for (int item = blockIdx.x; item < p.total; item += gridDim.x, ++it) {
+  for (int it = 0;; ++it) {
+    int item, nb;
+    {
+      Piece pc;
+      if (!piece_at<SPLIT>(p, it, pc)) break;
+      item = pc.item;
+      nb = pc.k1 - pc.k0;
+    }
     const Item wi = decode_item(p, item);
     const int srow = (2 * wi.pair + t) * kBM + r;
     uint64_t tr_q0 = 0, tr_q1 = 0, tr_e0 = 0;  // trace stamps (TRACE only)
@@ -640,7 +784,12 @@ __device__ void softmax_role(const Params& p, int t, uint32_t bar0, uint32_t tme
     float l = 0.f;
     BlockWalker<MODE> kb;
     kb.reset(p);
-    for (int j = 0; j < p.nblk; ++j) {
+    if constexpr (MODE != kModeS2S) {
+      Piece pc;
+      piece_at<SPLIT>(p, it, pc);
+      kb.b = pc.k0;  // (the split tail is not used with per-partition blocks)
+    }
+    for (int j = 0; j < nb; ++j) {  // the piece's key blocks, counted from its first
       const bool got = __all_sync(0xffffffffu, mbar_wait(BAR(C::SF + t), sf_cnt & 1, w));
       if (!got) return;
       ++sf_cnt;
@@ -700,6 +849,26 @@ __device__ void softmax_role(const Params& p, int t, uint32_t bar0, uint32_t tme
     if (!got) return;
     if constexpr (TRACE) tr_q1 = globaltimer_ns();
     tc_fence_after();
+    if constexpr (SPLIT) {
+      Piece pc;
+      piece_at<SPLIT>(p, it, pc);
+      if (pc.kind == 1) {
+        // a partial piece of a split item: its O goes to the workspace, no
+        // output; the staging buffer of the bulk-store epilogue is passed on in turn
+        write_partial<D>(p, t, r, lane, warp & 3, tO, m_used, l);
+        tc_fence_before();
+        mbar_arrive(BAR(C::OE + t));
+        if constexpr (kBulkStores<MODE>) {
+          const uint32_t u = 2u * static_cast<uint32_t>(it) + static_cast<uint32_t>(t);
+          if ((warp & 3) == 0 && lane == 0) {
+            if (u > 0 && !mbar_wait(BAR(C::STG), (u - 1) & 1u, w)) return;
+            mbar_arrive(BAR(C::STG));
+          }
+        }
+        continue;
+      }
+      if (pc.kind == 2 && !merge_partials<D>(p, item, t, r, warp & 3, tO, m_used, l, w)) return;
+    }
     uint32_t o[D];
     if constexpr (D == 128) tmem_ld_x128(tO, o);
     else tmem_ld_x64(tO, o);
@@ -789,7 +958,7 @@ __device__ void softmax_role(const Params& p, int t, uint32_t bar0, uint32_t tme
 }
 
 // ------------------------------------------------------------------ kernel
-template <int D, int MODE, int NMAP, bool TRACE = false>
+template <int D, int MODE, int NMAP, bool TRACE = false, bool SPLIT = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_tc_kernel(const __grid_constant__ Maps<NMAP> maps, const __grid_constant__ Params p) {
   using C = Cfg<D>;
@@ -844,20 +1013,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // a tail kernel queued behind this one may launch now: it takes each SM
+  // as this kernel's CTA there exits (no effect without one)
+  if constexpr (!SPLIT) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const WaitCtl w{abort_flag, p.dev_status, p.timeout_ns};
 
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
     if (warp == 0) {
-      if (lane == 0) producer_role<D, MODE, NMAP>(p, &maps, sbase, bar0, w);
+      if (lane == 0) producer_role<D, MODE, NMAP, SPLIT>(p, &maps, sbase, bar0, w);
     } else if (warp == 1) {
-      if (lane == 0) mma_role<D>(p, sbase, bar0, tmem, w);
+      if (lane == 0) mma_role<D, SPLIT>(p, sbase, bar0, tmem, w);
     } else if (warp == 2) {
-      if (lane == 0) relay_role<D>(p, sbase, bar0, w);
+      if (lane == 0) relay_role<D, SPLIT>(p, sbase, bar0, w);
     }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
-    softmax_role<D, MODE, NMAP, TRACE>(p, (warp - 4) / 4, bar0, tmem, &maps, sbase + C::STG_OFF, w);
+    softmax_role<D, MODE, NMAP, TRACE, SPLIT>(p, (warp - 4) / 4, bar0, tmem, &maps, sbase + C::STG_OFF, w);
     // the bulk-store issuers: every store must have completed before the CTA exits
     if (kBulkStores<MODE> && (warp & 3) == 0 && lane == 0) bulk_wait_all();
   }

@@ -8,7 +8,6 @@
 #include <cuda.h>
 #include <cstdint>
 
-#include "exp2_poly.cuh"
 #include "tmem_ops.cuh"
 
 namespace attn_a2a {
@@ -119,6 +118,32 @@ __device__ __forceinline__ bool counter_wait(uint32_t addr, uint32_t target, con
   }
   asm volatile("fence.acq_rel.cta;" ::: "memory");
   return true;
+}
+
+// Wait until the global word at `f` holds `want` (written with a release by
+// another CTA of this grid), then order the caller's later loads after it.
+// Bounded like mbar_wait: false on abort or after the time limit.
+__device__ __forceinline__ bool flag_wait(const unsigned* f, unsigned want, const WaitCtl& w) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+  if (v == want) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    __nanosleep(32);
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+    if (v == want) return true;
+    if ((it & 15u) == 0) {
+      if (*w.abort_flag) return false;
+      if (globaltimer_ns() - t0 > w.timeout_ns) {
+        raise_timeout(w);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void st_release_gpu_u32(unsigned* f, unsigned v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(f), "r"(v) : "memory");
 }
 
 // A wait used only while tearing down after an abort: ignores the abort flag,
@@ -298,29 +323,6 @@ __device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
   uint64_t r;
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
   return r;
-}
-
-// 2^x for two floats on the FMA pipe instead of the MUFU. Cody-Waite style
-// reduction x = j + f with j = rint(x): adding 1.5*2^23 leaves rint(x) in the
-// low mantissa bits of t (two's complement), so j = t - 1.5*2^23 and
-// f = x - j lies in [-1/2, 1/2]; 2^f comes from the minimax cubic of
-// exp2_poly.cuh and 2^j is applied by adding j << 23 to the result's bits.
-// x is clamped to >= -126 so that the exponent field cannot underflow; the
-// result is then below 2^-125, i.e. zero for every use here.
-__device__ __forceinline__ void exp2_poly_x2(float x0, float x1, float& y0, float& y1) {
-  constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
-  const uint64_t X = f2_pack(fmaxf(x0, -126.0f), fmaxf(x1, -126.0f));
-  const uint64_t T = f2_add(X, f2_pack(kRound, kRound));
-  const uint64_t J = f2_add(T, f2_pack(-kRound, -kRound));
-  const uint64_t F = f2_fma(J, f2_pack(-1.0f, -1.0f), X);
-  uint64_t P = f2_fma(F, f2_pack(kExp2C3, kExp2C3), f2_pack(kExp2C2, kExp2C2));
-  P = f2_fma(P, F, f2_pack(kExp2C1, kExp2C1));
-  P = f2_fma(P, F, f2_pack(kExp2C0, kExp2C0));
-  float p0, p1, t0, t1;
-  f2_unpack(P, p0, p1);
-  f2_unpack(T, t0, t1);
-  y0 = __int_as_float(__float_as_int(p0) + (__float_as_int(t0) << 23));
-  y1 = __int_as_float(__float_as_int(p1) + (__float_as_int(t1) << 23));
 }
 
 __device__ __forceinline__ float ex2_approx(float x) {

@@ -37,16 +37,28 @@ sys.path.insert(0, ROOT)
 METRIC = "fused attn+A2A-layout TFLOP/s and % of bf16 dense tensor peak, 1 GB300"
 WORKLOAD = "video DiT attention + Ulysses post-attention A2A layout: B=1, H=40, S=32768, d=128, P=8 virtual ranks"
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
-KERNEL_SOURCES = ["fa_tc.cuh", "ptx.cuh", "epilogue.cuh", "tmem_ops.cuh", "fa_tc.cu"]
+KERNEL_SOURCES = ["fa_tc.cuh", "ptx.cuh", "epilogue.cuh", "tmem_ops.cuh", "fa_tc.cu", "fa_tc_launch.cuh",
+                  "fa_tc_split.cu"]
 
 
-def fused_kernel_label(cfg) -> str:
+def split_tail_used(cfg, grid: int) -> bool:
+    """Whether a call with a workspace splits its last wave: fewer items than CTAs in it."""
+    npair = ((cfg.S + 127) // 128 + 1) // 2
+    total = cfg.B * cfg.H * npair
+    grid = min(grid, total)
+    waves = (total + grid - 1) // grid
+    return total - (waves - 1) * grid < grid and (cfg.S + 127) // 128 >= 2
+
+
+def fused_kernel_label(cfg, split: bool) -> str:
     """The kernel instantiation the fused call launches for cfg (the ncu name)."""
     from attention_all_layout_gb300 import binding as bd
 
     bulk = bd.attn_a2a_store_kind(cfg.S, cfg.P, 1) == 1
-    return (f"fa_fwd_tc_kernel<{cfg.d}, {3 if bulk else 1}, 1> (all-to-all layout, "
-            f"{'bulk-store' if bulk else 'row-store'} epilogue)")
+    split = split and split_tail_used(cfg, bd.num_sms())
+    return (f"fa_fwd_tc_kernel<{cfg.d}, {3 if bulk else 1}, 1, false, {'true' if split else 'false'}> "
+            f"(all-to-all layout, {'bulk-store' if bulk else 'row-store'} epilogue"
+            f"{', split tail' if split else ''})")
 
 
 def dist_env():
@@ -284,6 +296,8 @@ def main():
                     help="time only the fused call (no attention-alone, serial or e2e legs); for profiling")
     ap.add_argument("--H", type=int, default=None, help="override the head count (smaller profiling cases)")
     ap.add_argument("--S", type=int, default=None, help="override the sequence length (smaller profiling cases)")
+    ap.add_argument("--no-split", action="store_true",
+                    help="no split-tail workspace: a partial last wave of work items leaves CTAs idle")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -313,12 +327,14 @@ def main():
     parts = bd.alloc_partitions(cfg.B, cfg.S, cfg.H, cfg.d, cfg.P)
     o = torch.empty((cfg.B, cfg.H, cfg.S, cfg.d), dtype=torch.bfloat16, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    # split-tail workspace (a partial last wave of work items is divided over all CTAs)
+    ws = None if args.no_split else bd.alloc_workspace(cfg.d)
 
     def fused():
-        bd.attn_a2a_fwd(q, k, v, cfg.P, cfg.scale, parts, dev_status=status, stream=stream)
+        bd.attn_a2a_fwd(q, k, v, cfg.P, cfg.scale, parts, dev_status=status, stream=stream, workspace=ws)
 
     def contig():
-        bd.attn_a2a_fwd_contig(q, k, v, cfg.scale, o, dev_status=status, stream=stream)
+        bd.attn_a2a_fwd_contig(q, k, v, cfg.scale, o, dev_status=status, stream=stream, workspace=ws)
 
     def serial():
         contig()
@@ -358,7 +374,8 @@ def main():
             print(json.dumps({"metric": METRIC, "value": cfg.flops / (ms * 1e-3) / 1e12 * world,
                               "unit": "TFLOP/s", "ms_per_step": ms, "steps": args.steps,
                               "config": {"workload": cfg.name, "B": cfg.B, "H": cfg.H, "S": cfg.S,
-                                         "d": cfg.d, "P": cfg.P}, "clocks": clocks, "fused_only": True}),
+                                         "d": cfg.d, "P": cfg.P, "split_tail": ws is not None},
+                              "clocks": clocks, "fused_only": True}),
                   flush=True)
         return 0
     # ---- comparison legs, taking turns over three rounds (median per leg), so
@@ -452,12 +469,14 @@ def main():
         "config": {"workload": WORKLOAD if cfg.name == "video" else cfg.name, "B": cfg.B, "H": cfg.H,
                    "S": cfg.S, "d": cfg.d, "P": cfg.P,
                    "l2": "no flush: q,k,v inputs (%.2f GB) exceed the 129 MB L2" % (cfg.qkv_bytes / 1e9),
-                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU, P virtual ranks"},
+                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU, P virtual ranks",
+                   "split_tail": ws is not None},
         "pct_of_bf16_peak": 100.0 * tflops / peak,
         "pct_of_bf16_peak_sustained": 100.0 * tflops / peaks.get("bf16_tflops_sustained", peak),
         "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
                      "frac": tflops / peak, "traffic": traffic,
-                     "kernel": fused_kernel_label(cfg), "peak_source": f"{peak_src} bf16_tflops (burst)"},
+                     "kernel": fused_kernel_label(cfg, ws is not None),
+                     "peak_source": f"{peak_src} bf16_tflops (burst)"},
         "fused_in_turns_ms": ms_turns,
         "attention_alone_ms": ms_contig,
         "permute_ms": ms_permute,
@@ -470,7 +489,8 @@ def main():
                 "h2d_bytes_per_step": cfg.qkv_bytes, "d2h_bytes_per_step": cfg.out_bytes,
                 "ms_per_step": ms_e2e},
         "clocks": clocks,
-        "gpu_launches": args.steps,
+        # the split tail runs as a second kernel behind the first one
+        "gpu_launches": args.steps * (2 if ws is not None and split_tail_used(cfg, bd.num_sms()) else 1),
         "cpu_baseline": cpu,
     }
     print(json.dumps(line), flush=True)

@@ -132,7 +132,39 @@ typedef struct {
                            FlashAttention-A2A ("Key Contributions") from rank r's tile
                            owners into rank j's buffer */
   int reserved;
+  void* workspace;      /* NULL in normal use. Device scratch of at least
+                           ATTN_A2A_WORKSPACE_BYTES(grid, d) bytes (grid = the
+                           persistent CTAs, attn_a2a_num_sms() by default), 256-byte
+                           aligned, zeroed by the caller before its first use, not
+                           overlapping any input or output. With it, when the last wave
+                           of work items holds fewer items than there are CTAs and
+                           dividing it saves each CTA at least 32 key blocks (long
+                           sequences), that wave's key blocks are divided over all CTAs
+                           in a second kernel queued behind the first (programmatic
+                           dependent launch): a CTA whose range ends inside an item
+                           writes that item's partial result here; the CTA holding the
+                           item's last key block merges the partials and stores the tile.
+                           Otherwise the call is the same as without a workspace. The
+                           kernel leaves the workspace valid for the next call; calls
+                           that share one workspace must not run at the same time. Not
+                           used with tile_order = 1 or trace. The split items agree with
+                           the unsplit schedule to rounding (their key blocks are summed
+                           in pieces); all other items are the same bytes.
+                           attn_a2a_fwd_ex and attn_a2a_fwd_contig_ex only */
+  long long workspace_bytes; /* size of workspace */
 } attn_a2a_opts;
+
+/* Workspace bytes of attn_a2a_opts.workspace for a grid of `grid` CTAs and
+ * head dimension d: per CTA, a flag word per (query tile, warp), and one
+ * partial result (O fp32, running maximum, row sum) of two 128-row tiles. */
+#define ATTN_A2A_WORKSPACE_BYTES(grid, d) \
+  (256LL + 32LL * (long long)(grid) + 1024LL * (long long)(grid) * ((long long)(d) + 2))
+
+/* Trace record of attn_a2a_opts.trace: int64 per (work item, tile, warp), and
+ * the buffer size in bytes for B, H, S. */
+#define ATTN_A2A_TRACE_RECORD 8
+#define ATTN_A2A_TRACE_BYTES(B, H, S) \
+  ((long long)(B) * (H) * ((((long long)(S) + 127) / 128 + 1) / 2) * 2 * 4 * ATTN_A2A_TRACE_RECORD * 8)
 
 /*
  * attn_a2a_fwd - fused attention + head-to-sequence all-to-all (the product).

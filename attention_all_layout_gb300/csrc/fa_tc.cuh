@@ -34,12 +34,14 @@
 // place before it publishes P_t_j.
 //
 // Why a relay: on GB300 any shared-memory load or mbarrier query in the
-// thread that issues tcgen05.mma stalls it behind its queued MMAs (~170-220
-// cycles; measured with back-to-back 128x128x16 MMAs, which run at 64 cycles
-// each undisturbed). The issuer therefore syncs twice per key block - before
-// O1 += P1 V (P1 ready), and before O0 += P0 V together with the next S0
-// (V_j landed, P0 ready and K_{j+1} landed, one event) - and the relay thread
-// does the individual barrier waits.
+// thread that issues tcgen05.mma stalls it behind its queued MMAs. The issuer
+// therefore syncs twice per key block - before O1 += P1 V (P1 ready), and
+// before O0 += P0 V together with the next S0 (V_j landed, P0 ready and
+// K_{j+1} landed, one event) - and the relay thread does the individual
+// barrier waits. It hands each event over through an mbarrier, whose parity
+// wait measured cheaper in the issuer (about 55 cycles per sync between
+// groups of eight 128x128x16 MMAs) than a load of a shared-memory counter with
+// a branch on it (about 120).
 #pragma once
 
 #include <cuda.h>
@@ -90,10 +92,14 @@ struct Cfg {
   // tile epilogue, in the order tile 0, tile 1, tile 0, ...); STGW + t = the
   // four warps of tile t have written their rows
   static constexpr int STG = DONE + 1, STGW = DONE + 2;
-  static constexpr int NBAR = STGW + 2;
+  // relay -> MMA issuer events (one arrival each): EVA = A, EVB = B_j, EVC =
+  // C_j and E. Each kind's next event depends on MMAs issued after the issuer
+  // consumed the previous one, so no event barrier completes two phases ahead
+  // of the issuer's parity wait.
+  static constexpr int EVA = STGW + 2, EVB = EVA + 1, EVC = EVA + 2;
+  static constexpr int NBAR = EVC + 1;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
-  // MISC: +0 abort flag, +4 TMEM base, +8 relay event count
-  static constexpr int CNT_EV = MISC_OFF + 8;
+  // MISC: +0 abort flag, +4 TMEM base
   static constexpr int SMEM_USED = MISC_OFF + 16;
   static constexpr int SMEM_ALLOC = SMEM_USED + 1024;  // slack for 1024-byte alignment
   // the bulk-store epilogue's staging buffer: one 128-row output tile in
@@ -435,9 +441,8 @@ __device__ void mma_role(const Params& p, uint32_t sbase, uint32_t bar0, uint32_
   auto BAR = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
   constexpr uint32_t kIdescQK = idesc_bf16_f32(kBM, kBN, false, false);  // Q, K both K-major
   constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, D, false, true);     // V is MN-major (d contiguous)
-  const uint32_t cnt_ev = sbase + C::CNT_EV;
   uint32_t kv_it = 0;
-  uint32_t ev = 0;
+  uint32_t ev_a = 0, ev_b = 0, ev_c = 0;  // events consumed per kind
   bool ok = true;
 
   auto issue_qk = [&](int t, uint32_t sK) {
@@ -463,8 +468,9 @@ __device__ void mma_role(const Params& p, uint32_t sbase, uint32_t bar0, uint32_
     if (t == 1) umma_commit(BAR(C::KVE + sV));  // V_j now read by both tiles
     if (j == nb - 1) umma_commit(BAR(C::OF + t));
   };
-  auto sync = [&]() -> bool {
-    if (!counter_wait(cnt_ev, ++ev, w)) return false;
+  // wait for the relay's next event of one kind (its barrier's next phase)
+  auto sync = [&](int bar, uint32_t& n) -> bool {
+    if (!mbar_wait(BAR(bar), n++ & 1u, w)) return false;
     tc_fence_after();
     return true;
   };
@@ -474,13 +480,13 @@ __device__ void mma_role(const Params& p, uint32_t sbase, uint32_t bar0, uint32_
     if (!piece_at<SPLIT>(p, it, pc)) break;
     const int nb = pc.k1 - pc.k0;
     uint32_t sVprev = 0;
-    if (!sync()) { ok = false; break; }  // A: both Q tiles and the piece's first K
+    if (!sync(C::EVA, ev_a)) { ok = false; break; }  // A: both Q tiles and the piece's first K
     issue_qk(0, kv_it % C::NSTAGE);
     umma_commit(BAR(C::SF + 0));
     for (int j = 0; j < nb; ++j) {  // the piece's key blocks, counted from its first
       const uint32_t sK = kv_it % C::NSTAGE;
       if (j > 0) {
-        if (!sync()) { ok = false; break; }  // C_j: P1_{j-1} (and O1 free at j = 1)
+        if (!sync(C::EVC, ev_c)) { ok = false; break; }  // C_j: P1_{j-1} (and O1 free at j = 1)
         issue_pv(1, j - 1, sVprev, nb);
       }
       issue_qk(1, sK);
@@ -494,7 +500,7 @@ __device__ void mma_role(const Params& p, uint32_t sbase, uint32_t bar0, uint32_
       const uint32_t sV = kv_it % C::NSTAGE;
       // B_j: V_j and P0_j (and O0 free at j = 0), and K_{j+1}, so that
       // O0 += P0 V_j and S0_{j+1} go to the tensor core back to back
-      if (!sync()) { ok = false; break; }
+      if (!sync(C::EVB, ev_b)) { ok = false; break; }
       issue_pv(0, j, sV, nb);
       sVprev = sV;
       ++kv_it;
@@ -503,7 +509,7 @@ __device__ void mma_role(const Params& p, uint32_t sbase, uint32_t bar0, uint32_
         umma_commit(BAR(C::SF + 0));
       }
     }
-    if (ok && !sync()) ok = false;  // E: P1 of the last block (and O1 free if there is one block)
+    if (ok && !sync(C::EVC, ev_c)) ok = false;  // E: P1 of the last block (and O1 free if there is one block)
     if (ok) issue_pv(1, nb - 1, sVprev, nb);
   }
   if (!ok) {
@@ -528,8 +534,7 @@ template <int D, bool SPLIT>
 __device__ void relay_role(const Params& p, uint32_t sbase, uint32_t bar0, const WaitCtl& w) {
   using C = Cfg<D>;
   auto BAR = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
-  const uint32_t cnt_ev = sbase + C::CNT_EV;
-  uint32_t kv_it = 0, ev = 0;
+  uint32_t kv_it = 0;
   uint32_t pf_cnt[2] = {0, 0};
   int it = 0;
   auto kv_ready = [&]() -> bool {
@@ -543,21 +548,21 @@ __device__ void relay_role(const Params& p, uint32_t sbase, uint32_t bar0, const
     const int nb = pc.k1 - pc.k0;
     if (!(mbar_wait(BAR(C::QF + 0), it & 1, w) && mbar_wait(BAR(C::QF + 1), it & 1, w))) return;
     if (!kv_ready()) return;
-    st_release_u32(cnt_ev, ++ev);  // A
+    mbar_arrive(BAR(C::EVA));  // A
     for (int j = 0; j < nb; ++j) {
       if (j > 0) {
         if (!p_ready(1)) return;
         if (j == 1 && !o_free(1)) return;
-        st_release_u32(cnt_ev, ++ev);  // C_j
+        mbar_arrive(BAR(C::EVC));  // C_j
       }
       if (!kv_ready() || !p_ready(0)) return;  // V_j, P0_j
       if (j == 0 && !o_free(0)) return;
       if (j + 1 < nb && !kv_ready()) return;  // K_{j+1}
-      st_release_u32(cnt_ev, ++ev);  // B_j
+      mbar_arrive(BAR(C::EVB));  // B_j
     }
     if (!p_ready(1)) return;
     if (nb == 1 && !o_free(1)) return;
-    st_release_u32(cnt_ev, ++ev);  // E
+    mbar_arrive(BAR(C::EVC));  // E
   }
 }
 
@@ -989,8 +994,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(BAR(C::STG), 1);
     mbar_init(BAR(C::STGW + 0), 4);  // one arrive per warp of the tile
     mbar_init(BAR(C::STGW + 1), 4);
+    mbar_init(BAR(C::EVA), 1);
+    mbar_init(BAR(C::EVB), 1);
+    mbar_init(BAR(C::EVC), 1);
     *abort_flag = 0;
-    reinterpret_cast<uint32_t*>(sgen + C::MISC_OFF)[2] = 0;  // relay event count
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {

@@ -85,17 +85,18 @@ struct Cfg {
   static constexpr int KV_OFF = 2 * TILE_BYTES;
   static constexpr int BAR_OFF = KV_OFF + NSTAGE * TILE_BYTES;
   // barrier slots
-  static constexpr int QF = 0, QE = 2, SF = 4, PF = 6, OF = 8, OE = 10, KVF = 12;
+  static constexpr int QF = 0, QE = 2, SF = 4, OF = 6, OE = 8, KVF = 10;
   static constexpr int KVE = KVF + NSTAGE;
   static constexpr int DONE = KVE + NSTAGE;
   // bulk-store epilogue: STG = the staging buffer is free again (one phase per
   // tile epilogue, in the order tile 0, tile 1, tile 0, ...); STGW + t = the
   // four warps of tile t have written their rows
   static constexpr int STG = DONE + 1, STGW = DONE + 2;
-  // relay -> MMA issuer events (one arrival each): EVA = A, EVB = B_j, EVC =
-  // C_j and E. Each kind's next event depends on MMAs issued after the issuer
-  // consumed the previous one, so no event barrier completes two phases ahead
-  // of the issuer's parity wait.
+  // the MMA issuer's events (see relay_role): EVA = A (the relay's arrival),
+  // EVB = B_j (tile 0's 128 softmax threads + the relay), EVC = C_j and E
+  // (tile 1's 128 softmax threads + the relay). Each kind's next event depends
+  // on MMAs issued after the issuer consumed the previous one, so no event
+  // barrier completes two phases ahead of the issuer's parity wait.
   static constexpr int EVA = STGW + 2, EVB = EVA + 1, EVC = EVA + 2;
   static constexpr int NBAR = EVC + 1;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
@@ -520,30 +521,40 @@ __device__ void mma_role(const Params& p, uint32_t sbase, uint32_t bar0, uint32_
 }
 
 // ------------------------------------------------------------------ relay
-// Does the MMA issuer's fine-grained waits (TMA barriers, P ready, O free)
-// in its issue order and publishes one event per group of MMAs that may go:
-//   A    both Q tiles and K_0 landed (once per item)         -> S0_0
-//   C_j  P1_{j-1} ready (and O1 free at j = 1), j > 0        -> O1 += P1 V, S1_j
-//   B_j  V_j landed, P0_j ready (and O0 free at j = 0), and
-//        K_{j+1} landed unless j is the last block           -> O0 += P0 V, S0_{j+1}
-//   E    P1 of the last block ready (and O1 free if one block) -> last O1 += P1 V
-// Each wait depends only on MMAs issued before the event it gates, and the
-// softmax roles cannot run a barrier two phases ahead of these parity waits
-// (their next phase needs an S that is only issued after the relay's event).
+// Completes the MMA issuer's events, one barrier phase per event, in issue
+// order:
+//   A    EVA, the relay's arrival: both Q tiles and the piece's first K landed -> S0_0
+//   C_j  EVC, tile 1's 128 softmax threads (P1_{j-1} written) and the relay
+//        (O1 free at j = 1), j > 0                                 -> O1 += P1 V, S1_j
+//   B_j  EVB, tile 0's 128 softmax threads (P0_j written) and the relay (V_j
+//        landed, O0 free at j = 0, K_{j+1} landed unless j is last) -> O0 += P0 V, S0_{j+1}
+//   E    EVC, tile 1's softmax threads (P1 of the last block) and the relay
+//        (O1 free if the piece has one block)                      -> last O1 += P1 V
+// The probabilities' readiness thus reaches the issuer in one hop, while the
+// relay takes the waits on the TMA and O-free barriers off the issuer. The
+// relay arrives for an event only once the barrier's previous phase has
+// completed, so its arrival cannot count toward the previous event; the
+// softmax threads' arrivals for an event need an S that is issued only after
+// the issuer consumed the previous one, so they cannot either.
 template <int D, bool SPLIT>
-__device__ void relay_role(const Params& p, uint32_t sbase, uint32_t bar0, const WaitCtl& w) {
+__device__ void relay_role(const Params& p, uint32_t bar0, const WaitCtl& w) {
   using C = Cfg<D>;
   auto BAR = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
   uint32_t kv_it = 0;
-  uint32_t pf_cnt[2] = {0, 0};
+  uint32_t n_b = 0, n_c = 0;  // EVB / EVC events arrived for so far
   int it = 0;
   auto kv_ready = [&]() -> bool {
     const bool r = mbar_wait(BAR(C::KVF + kv_it % C::NSTAGE), (kv_it / C::NSTAGE) & 1, w);
     ++kv_it;
     return r;
   };
-  auto p_ready = [&](int t) -> bool { return mbar_wait(BAR(C::PF + t), pf_cnt[t]++ & 1, w); };
   auto o_free = [&](int t) -> bool { return mbar_wait(BAR(C::OE + t), (it & 1) ^ 1, w); };
+  // before arriving for an event of a barrier: its previous phase has completed
+  auto after_previous = [&](int bar, uint32_t& n) -> bool {
+    const bool r = n == 0 || mbar_wait(BAR(bar), (n - 1) & 1u, w);
+    ++n;
+    return r;
+  };
   for (Piece pc; piece_at<SPLIT>(p, it, pc); ++it) {
     const int nb = pc.k1 - pc.k0;
     if (!(mbar_wait(BAR(C::QF + 0), it & 1, w) && mbar_wait(BAR(C::QF + 1), it & 1, w))) return;
@@ -551,16 +562,17 @@ __device__ void relay_role(const Params& p, uint32_t sbase, uint32_t bar0, const
     mbar_arrive(BAR(C::EVA));  // A
     for (int j = 0; j < nb; ++j) {
       if (j > 0) {
-        if (!p_ready(1)) return;
+        if (!after_previous(C::EVC, n_c)) return;
         if (j == 1 && !o_free(1)) return;
         mbar_arrive(BAR(C::EVC));  // C_j
       }
-      if (!kv_ready() || !p_ready(0)) return;  // V_j, P0_j
+      if (!after_previous(C::EVB, n_b)) return;
+      if (!kv_ready()) return;  // V_j
       if (j == 0 && !o_free(0)) return;
       if (j + 1 < nb && !kv_ready()) return;  // K_{j+1}
       mbar_arrive(BAR(C::EVB));  // B_j
     }
-    if (!p_ready(1)) return;
+    if (!after_previous(C::EVC, n_c)) return;
     if (nb == 1 && !o_free(1)) return;
     mbar_arrive(BAR(C::EVC));  // E
   }
@@ -847,7 +859,9 @@ __device__ void softmax_role(const Params& p, int t, uint32_t bar0, uint32_t tme
       l += ls;
       tmem_st_x64(tS, pk);
       tc_fence_before();
-      if (!(p.inject_stall && t == 0 && j == 0 && it == 0)) mbar_arrive(BAR(C::PF + t));  // test hook
+      // P_t written: this thread's arrival on the issuer's event (B_j for tile 0,
+      // C_{j+1} or E for tile 1)
+      if (!(p.inject_stall && t == 0 && j == 0 && it == 0)) mbar_arrive(BAR(t == 0 ? C::EVB : C::EVC));  // test hook
     }
     // ---- epilogue: the tile owner stores its rows to their destination and moves on
     const bool got = __all_sync(0xffffffffu, mbar_wait(BAR(C::OF + t), it & 1, w));
@@ -982,7 +996,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(BAR(C::QF + t), 1);
       mbar_init(BAR(C::QE + t), 1);
       mbar_init(BAR(C::SF + t), 1);
-      mbar_init(BAR(C::PF + t), kBM);
       mbar_init(BAR(C::OF + t), 1);
       mbar_init(BAR(C::OE + t), kBM);
     }
@@ -995,8 +1008,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(BAR(C::STGW + 0), 4);  // one arrive per warp of the tile
     mbar_init(BAR(C::STGW + 1), 4);
     mbar_init(BAR(C::EVA), 1);
-    mbar_init(BAR(C::EVB), 1);
-    mbar_init(BAR(C::EVC), 1);
+    mbar_init(BAR(C::EVB), kBM + 1);
+    mbar_init(BAR(C::EVC), kBM + 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -1032,7 +1045,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
       if (lane == 0) mma_role<D, SPLIT>(p, sbase, bar0, tmem, w);
     } else if (warp == 2) {
-      if (lane == 0) relay_role<D, SPLIT>(p, sbase, bar0, w);
+      if (lane == 0) relay_role<D, SPLIT>(p, bar0, w);
     }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));

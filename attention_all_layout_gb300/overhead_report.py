@@ -139,13 +139,13 @@ def traced_summary(fn, B, H, S):
     return out
 
 
-def report(H=40, d=128, P=8):
+def report(H=40, d=128, P=8, s_list=S_LIST):
     R, table = fit_store_model()
     R_b, table_b, held_b = fit_store_model_mma(kind=1)
     R_r, table_r, held_r = fit_store_model_mma(kind=0)
     n_sm = bd.num_sms()
     rows = []
-    for S in S_LIST:
+    for S in s_list:
         cfg = workloads.AttnConfig(f"S{S}", B=1, H=H, S=S, d=d, P=P)
         q, k, v = workloads.make_qkv(cfg, seed=0, device="cuda")
         parts = bd.alloc_partitions(1, S, H, d, P)

@@ -14,6 +14,8 @@ Prints one JSON line. Legs:
   cpu_baseline the float64 oracle on a bounded row sample, on host cores
   attention-alone, serial (attention, then a separate permute) and whole-layer
                times, taken in turns with the fused call over three rounds
+  other_presets_fused  the fused call on the image, joint and long presets
+               (CUDA events; context, not the headline)
 `--impl reference` times the oracle arm instead (CPU, rank 0 only).
 Multi-GPU (torchrun): every rank runs an independent replica of the workload
 (no data-path collective); value is the sum over ranks / slowest rank's time.
@@ -296,6 +298,7 @@ def main():
                     help="time only the fused call (no attention-alone, serial or e2e legs); for profiling")
     ap.add_argument("--H", type=int, default=None, help="override the head count (smaller profiling cases)")
     ap.add_argument("--S", type=int, default=None, help="override the sequence length (smaller profiling cases)")
+    ap.add_argument("--no-presets", action="store_true", help="skip timing the image, joint and long presets")
     ap.add_argument("--no-split", action="store_true",
                     help="no split-tail workspace: a partial last wave of work items leaves CTAs idle")
     args = ap.parse_args()
@@ -427,6 +430,23 @@ def main():
     f1.record(stream)
     barrier()
     ms_e2e = f0.elapsed_time(f1) / e2e_steps
+    del hq, hk, hv, dq, dk, dv, dparts, hparts
+
+    # ---- the other presets' fused call (context beside the headline; not the metric)
+    presets = {}
+    if cfg.name == "video" and not args.no_presets:
+        for name in ("image", "joint", "long"):
+            pc = workloads.CONFIGS[name]
+            pq, pk, pv = workloads.make_qkv(pc, seed=rank, device="cuda")
+            pparts = bd.alloc_partitions(pc.B, pc.S, pc.H, pc.d, pc.P)
+            pws = None if args.no_split else bd.alloc_workspace(pc.d)
+            n = 50 if pc.flops < 1e12 else 5
+            pms = time_events(lambda: bd.attn_a2a_fwd(pq, pk, pv, pc.P, pc.scale, pparts, dev_status=status,
+                                                      stream=stream, workspace=pws), n, 3, stream)
+            presets[name] = {"ms": pms, "tflops": pc.flops / (pms * 1e-3) / 1e12, "steps": n,
+                             "shape": {"B": pc.B, "H": pc.H, "S": pc.S, "d": pc.d, "P": pc.P}}
+            del pq, pk, pv, pparts, pws
+            torch.cuda.empty_cache()
     sampler.stop()
 
     peaks, peak_src = load_peaks()
@@ -492,6 +512,7 @@ def main():
         # the split tail runs as a second kernel behind the first one
         "gpu_launches": args.steps * (2 if ws is not None and split_tail_used(cfg, bd.num_sms()) else 1),
         "cpu_baseline": cpu,
+        "other_presets_fused": presets or None,
     }
     print(json.dumps(line), flush=True)
     if world > 1:

@@ -88,38 +88,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
   }
 }
 
-// Readiness handed to the MMA issuer through a counter in shared memory.
-// Every shared-memory load (or mbarrier query) in the issuing thread stalls
-// behind its queued MMAs (~170-220 cycles), so the issuer syncs as rarely as
-// the data dependencies allow and a relay thread does the fine-grained waits.
-__device__ __forceinline__ void st_release_u32(uint32_t addr, uint32_t v) {
-  asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-
-// Wait until the counter at `addr` reaches `target` (wrap-around safe), then
-// order everything after it behind the release that published the count.
-// Bounded like mbar_wait: false on abort or after the time limit.
-__device__ __forceinline__ bool counter_wait(uint32_t addr, uint32_t target, const WaitCtl& w) {
-  uint32_t v;
-  asm volatile("ld.volatile.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-  if (static_cast<int32_t>(v - target) < 0) {
-    const uint64_t t0 = globaltimer_ns();
-    for (uint32_t it = 1;; ++it) {
-      asm volatile("ld.volatile.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-      if (static_cast<int32_t>(v - target) >= 0) break;
-      if ((it & 63u) == 0) {
-        if (*w.abort_flag) return false;
-        if (globaltimer_ns() - t0 > w.timeout_ns) {
-          raise_timeout(w);
-          return false;
-        }
-      }
-    }
-  }
-  asm volatile("fence.acq_rel.cta;" ::: "memory");
-  return true;
-}
-
 // Wait until the global word at `f` holds `want` (written with a release by
 // another CTA of this grid), then order the caller's later loads after it.
 // Bounded like mbar_wait: false on abort or after the time limit.

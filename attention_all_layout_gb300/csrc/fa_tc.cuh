@@ -13,8 +13,9 @@
 //   warp 0      TMA producer: Q tiles once per work item, then K_j, V_j
 //               through a ring of shared-memory stages
 //   warp 1      MMA issuer (one thread) and TMEM allocator
-//   warp 2      relay: waits on the TMA, P-ready and O-free barriers on the
-//               issuer's behalf and hands it one event per group of MMAs
+//   warp 2      relay: waits on the TMA and O-free barriers on the issuer's
+//               behalf; with the softmax threads' own arrivals it completes
+//               one event barrier phase per group of MMAs
 //   warp 3      idle
 //   warps 4-7   softmax/correction/epilogue for query tile 0 (128 rows)
 //   warps 8-11  the same for query tile 1
@@ -37,11 +38,12 @@
 // thread that issues tcgen05.mma stalls it behind its queued MMAs. The issuer
 // therefore syncs twice per key block - before O1 += P1 V (P1 ready), and
 // before O0 += P0 V together with the next S0 (V_j landed, P0 ready and
-// K_{j+1} landed, one event) - and the relay thread does the individual
-// barrier waits. It hands each event over through an mbarrier, whose parity
-// wait measured cheaper in the issuer (about 55 cycles per sync between
-// groups of eight 128x128x16 MMAs) than a load of a shared-memory counter with
-// a branch on it (about 120).
+// K_{j+1} landed, one event) - each on one mbarrier phase. The relay thread
+// does the waits on the TMA and O-free barriers and arrives on the event's
+// barrier; the softmax threads that wrote P arrive on it directly. A parity
+// wait on an mbarrier measured cheaper in the issuer (about 55 cycles per
+// sync between groups of eight 128x128x16 MMAs) than a load of a
+// shared-memory counter with a branch on it (about 120).
 #pragma once
 
 #include <cuda.h>

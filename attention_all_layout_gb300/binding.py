@@ -55,7 +55,7 @@ class Opts(ctypes.Structure):
         ("tile_order", ctypes.c_int),
         ("trace", ctypes.c_void_p),
         ("part_heads", ctypes.c_int),
-        ("reserved", ctypes.c_int),
+        ("split", ctypes.c_int),
         ("workspace", ctypes.c_void_p),
         ("workspace_bytes", ctypes.c_longlong),
     ]
@@ -191,10 +191,13 @@ def _ptr_array(tensors: Sequence):
     return arr
 
 
+SPLIT_AUTO, SPLIT_TAIL, SPLIT_ALL, SPLIT_NONE = 0, 1, 2, 3  # attn_a2a_opts.split
+
+
 def _opts(store_kind=0, grid=0, timeout_ns=0, inject_stall=0, tile_order=0, trace=None, part_heads=0,
-          workspace=None) -> Opts:
+          workspace=None, split=SPLIT_AUTO) -> Opts:
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    return Opts(store_kind, grid, timeout_ns, inject_stall, tile_order, _ptr(trace), part_heads, 0,
+    return Opts(store_kind, grid, timeout_ns, inject_stall, tile_order, _ptr(trace), part_heads, split,
                 _ptr(workspace), ws_bytes)
 
 
@@ -238,30 +241,32 @@ def _check(code: int, what: str, check: bool) -> int:
 # ------------------------------------------------------------------ entry points (same names as the C ABI)
 def attn_a2a_fwd(q, k, v, P: int, scale: float, out_partitions, dev_status=None, stream=None,
                  store_kind: int = 0, grid: int = 0, timeout_ns: int = 0, inject_stall: int = 0,
-                 tile_order: int = 0, trace=None, part_heads: int = 0, workspace=None, check: bool = True) -> int:
+                 tile_order: int = 0, trace=None, part_heads: int = 0, workspace=None, split: int = SPLIT_AUTO,
+                 check: bool = True) -> int:
     """Fused attention + head->sequence all-to-all into `out_partitions` (P tensors [B,c_j,H,d]).
     trace: optional device int64 tensor of trace_numel(B, H, S) elements for per-tile stamps.
     part_heads: heads per partition row for a head-group launch (0 = H); the partitions are then
     given as device addresses already offset to the group's first head (see ulysses.py).
-    workspace: optional zeroed uint8 tensor (alloc_workspace) that lets a partial last wave of
-    work items be split over all CTAs."""
+    workspace: optional zeroed uint8 tensor (alloc_workspace) that lets work items be split over
+    all CTAs by key blocks; split: which (SPLIT_AUTO, SPLIT_TAIL, SPLIT_ALL, SPLIT_NONE)."""
     lib = load()
     shp = shape_of(q, k, v)
     parts = _ptr_array(out_partitions)
     _check_trace(trace, shp)
-    opts = _opts(store_kind, grid, timeout_ns, inject_stall, tile_order, trace, part_heads, workspace)
+    opts = _opts(store_kind, grid, timeout_ns, inject_stall, tile_order, trace, part_heads, workspace, split)
     rc = lib.attn_a2a_fwd_ex(_ptr(q), _ptr(k), _ptr(v), ctypes.byref(shp), int(P), float(scale), parts,
                              _ptr(dev_status), ctypes.byref(opts), _stream(stream))
     return _check(rc, "attn_a2a_fwd", check)
 
 
 def attn_a2a_fwd_contig(q, k, v, scale: float, out, dev_status=None, stream=None, store_kind: int = 0,
-                        grid: int = 0, timeout_ns: int = 0, trace=None, workspace=None, check: bool = True) -> int:
+                        grid: int = 0, timeout_ns: int = 0, trace=None, workspace=None, split: int = SPLIT_AUTO,
+                        check: bool = True) -> int:
     """The same kernel with a contiguous [B, H, S, d] output ("attention alone")."""
     lib = load()
     shp = shape_of(q, k, v)
     _check_trace(trace, shp)
-    opts = _opts(store_kind, grid, timeout_ns, 0, 0, trace, 0, workspace)
+    opts = _opts(store_kind, grid, timeout_ns, 0, 0, trace, 0, workspace, split)
     rc = lib.attn_a2a_fwd_contig_ex(_ptr(q), _ptr(k), _ptr(v), ctypes.byref(shp), float(scale), _ptr(out),
                                     _ptr(dev_status), ctypes.byref(opts), _stream(stream))
     return _check(rc, "attn_a2a_fwd_contig", check)

@@ -24,6 +24,18 @@ int num_sms_current_device() {
   return cache[dev];
 }
 
+long long l2_bytes_current_device() {
+  static long long cache[128] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return 0;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrL2CacheSize, dev) != cudaSuccess) return 0;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
 namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -181,7 +193,8 @@ int fwd_common(const void* q, const void* k, const void* v, const attn_a2a_shape
                           opts->timeout_ns < 0 || opts->inject_stall < 0 || opts->inject_stall > 1 ||
                           opts->tile_order < 0 || opts->tile_order > 1 ||
                           (reinterpret_cast<uintptr_t>(opts->trace) & 7u) != 0 || opts->part_heads < 0 ||
-                          (opts->part_heads > 0 && !a2a)))
+                          (opts->part_heads > 0 && !a2a) || opts->split < ATTN_A2A_SPLIT_AUTO ||
+                          opts->split > ATTN_A2A_SPLIT_NONE))
     return ATTN_A2A_EINVAL;
   // the bulk-store epilogue exists for the contiguous layout and for the
   // all-to-all layout with up to 8 partitions

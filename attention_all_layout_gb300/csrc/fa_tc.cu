@@ -121,33 +121,63 @@ unsigned next_epoch() {
 }
 
 // Fewest key blocks per CTA that a split tail must save over the unsplit last
-// wave (nblk - tail_len) before it is used. A tail piece restarts the
-// two-tile pipeline (Q loads, first block, drain) and a split item pays for
-// its partials' writes and merge: measured on GB300, a tail of 17-block ranges
-// instead of 32-block items (the image preset) ran 42 us without the merge
-// instead of about 30, and the partials' write and merge added about 17 us,
-// so that the split lost 6 % there (joint, 31 of 36 blocks: lost 10 %); at
-// the video and long presets (80 and 62 blocks saved) it gained 0.3-0.8 %.
+// wave (nblk - tail_len) before the automatic choice uses it. A tail piece
+// restarts the two-tile pipeline (Q loads, first block, drain) and a split
+// item pays for its partials' writes and merge: measured on GB300, a tail of
+// 17-block ranges instead of 32-block items (the image preset) ran 42 us
+// without the merge instead of about 30, and the partials' write and merge
+// added about 17 us, so that the split lost 6 % there (joint, 31 of 36
+// blocks: lost 10 %); at the video and long presets (80 and 62 blocks saved)
+// it gained 0.3-0.8 %.
 constexpr int kSplitMinSavedBlocks = 32;
 
-// Split tail (the kernel's tail_piece): when the last wave holds r < grid
-// items, its r * nblk key blocks are divided into ranges of
-// ceil(r * nblk / grid) <= nblk blocks, one per CTA, if that saves at least
-// kSplitMinSavedBlocks blocks per CTA. Needs the caller's workspace; returns
-// ATTN_A2A_EINVAL if it is too small.
-int plan_split_tail(tc::Params& p, int grid, int d, const attn_a2a_opts& opts) {
+// Fewest key blocks per CTA that the whole-schedule split must save over the
+// unsplit waves before the automatic choice uses it, and only where the K and
+// V of every head fit in half of L2: its ranges walk through all heads at
+// once, so with more K/V than L2 holds every range re-reads its heads' K and
+// V from HBM (measured on GB300: video and long presets 20 % slower). A cut
+// item costs a partial write (3.6 us) and a merge (2-3 us) on the critical
+// path: measured, the image preset (15 blocks saved of 96) ran 8.5 % faster,
+// the joint preset (5 of 108) 1.5 % faster.
+constexpr int kSplitAllMinSavedBlocks = 4;
+
+// Split schedule (the kernel's tail_piece), with the caller's workspace:
+// ATTN_A2A_SPLIT_TAIL divides a last wave of r < grid items into ranges of
+// ceil(r * nblk / grid) <= nblk key blocks, one per CTA, run by a second
+// kernel behind the plain one; ATTN_A2A_SPLIT_ALL divides all items into
+// ranges of ceil(total * nblk / grid) blocks in one kernel (whole = true);
+// ATTN_A2A_SPLIT_AUTO takes the whole-schedule split where K and V fit in
+// half of L2 and it saves at least kSplitAllMinSavedBlocks blocks per CTA,
+// else the tail split where that saves at least kSplitMinSavedBlocks blocks
+// per CTA. Every range's CTA must be resident
+// at once (a final piece waits for other ranges), so a grid larger than the
+// SM count is not split. Returns ATTN_A2A_EINVAL if the workspace is too small.
+int plan_split_tail(tc::Params& p, int grid, int d, const attn_a2a_opts& opts, bool& whole) {
   p.tail_first = p.total;
   p.tail_len = 0;
-  if (opts.workspace == nullptr) return ATTN_A2A_OK;
+  whole = false;
+  if (opts.workspace == nullptr || opts.split == ATTN_A2A_SPLIT_NONE) return ATTN_A2A_OK;
   if (opts.workspace_bytes < ATTN_A2A_WORKSPACE_BYTES(grid, d)) return ATTN_A2A_EINVAL;
   if (opts.trace != nullptr || p.interleave > 1 || p.nblk < 2 || p.nblk > (1 << 20)) return ATTN_A2A_OK;
+  const long long blocks = static_cast<long long>(p.total) * p.nblk;
+  if (blocks > INT_MAX / 2 || grid > num_sms_current_device()) return ATTN_A2A_OK;
   const int waves = (p.total + grid - 1) / grid;
-  const int r = p.total - (waves - 1) * grid;
-  if (r >= grid) return ATTN_A2A_OK;  // the last wave is full
-  const int len = static_cast<int>((static_cast<long long>(r) * p.nblk + grid - 1) / grid);
-  if (p.nblk - len < kSplitMinSavedBlocks) return ATTN_A2A_OK;
-  p.tail_first = (waves - 1) * grid;
-  p.tail_len = len;
+  const int all_len = static_cast<int>((blocks + grid - 1) / grid);
+  const long long kv_bytes = 4LL * p.B * p.H * p.S * d;  // bf16 K and V of every head
+  const bool all_pays = 2 * kv_bytes <= l2_bytes_current_device() &&
+                        waves * p.nblk - all_len >= kSplitAllMinSavedBlocks;
+  if (opts.split == ATTN_A2A_SPLIT_ALL || (opts.split == ATTN_A2A_SPLIT_AUTO && all_pays)) {
+    p.tail_first = 0;
+    p.tail_len = all_len;
+    whole = true;
+  } else {
+    const int r = p.total - (waves - 1) * grid;
+    if (r >= grid) return ATTN_A2A_OK;  // the last wave is full
+    const int len = static_cast<int>((static_cast<long long>(r) * p.nblk + grid - 1) / grid);
+    if (opts.split == ATTN_A2A_SPLIT_AUTO && p.nblk - len < kSplitMinSavedBlocks) return ATTN_A2A_OK;
+    p.tail_first = (waves - 1) * grid;
+    p.tail_len = len;
+  }
   uint8_t* base = static_cast<uint8_t*>(opts.workspace);
   const size_t flags = (static_cast<size_t>(grid) * 32u + 255u) / 256u * 256u;
   p.ws_flags = reinterpret_cast<unsigned*>(base);
@@ -202,13 +232,15 @@ int launch_fa_tc(const void* q, const void* k, const void* v, const attn_a2a_sha
     p.interleave = epi.cbase / (2 * tc::kBM);
   const int grid = grid_for(p, opts);
   if (grid <= 0) return ATTN_A2A_ECUDA;
-  const int split_rc = plan_split_tail(p, grid, shp.d, opts);
+  bool whole = false;
+  const int split_rc = plan_split_tail(p, grid, shp.d, opts, whole);
   if (split_rc != ATTN_A2A_OK) return split_rc;
   const int mode = a2a ? (bulk ? tc::kModeA2AT : tc::kModeA2A) : (bulk ? tc::kModeContigT : tc::kModeContig);
   if (opts.trace != nullptr) {
     p.trace = opts.trace;
     return launch_fa_tc_traced(maps, p, shp.d, mode, grid, stream);
   }
+  if (whole) return launch_fa_tc_split(maps, p, shp.d, mode, grid, stream, false);
   if (p.tail_first < p.total) {
     // the full waves in the plain kernel, then the tail kernel behind it
     tc::Params pm = p;
@@ -216,7 +248,7 @@ int launch_fa_tc(const void* q, const void* k, const void* v, const attn_a2a_sha
     pm.tail_first = pm.total;
     const int rc = launch_plain(maps, pm, shp.d, mode, grid, stream);
     if (rc != ATTN_A2A_OK) return rc;
-    return launch_fa_tc_split(maps, p, shp.d, mode, grid, stream);
+    return launch_fa_tc_split(maps, p, shp.d, mode, grid, stream, true);
   }
   return launch_plain(maps, p, shp.d, mode, grid, stream);
 }

@@ -172,9 +172,10 @@ struct Params {
   int interleave;        // > 1: chunk-interleaved item order with this many pairs per chunk
   int seg;               // kModeS2SG(T): rows per TMA box of the sequence-sharded loads (128 or 64)
   long long* trace;      // traced instantiations only: kTraceRecord int64 per (item, tile, warp)
-  // Split tail (see tail_pieces): items [tail_first, total) are divided over
-  // the CTAs by key blocks, tail_len blocks per CTA; tail_first = total when
-  // the tail is not split. Partial results go through the caller's workspace.
+  // Split schedule (see tail_piece): the key blocks of items [tail_first,
+  // total) are divided over the CTAs, tail_len blocks per CTA; tail_first =
+  // total when nothing is split. Partial results go through the caller's
+  // workspace, one slot per range.
   int tail_first, tail_len;
   unsigned epoch;        // this launch's id, written to the workspace flags
   float* ws_o;           // [grid][2 tiles][D/4][128 rows] float4: a partial piece's O (unnormalised);
@@ -263,57 +264,53 @@ struct Item {
   int b, h, pair;
 };
 
-// ------------------------------------------------------------------ split tail
-// The last wave of work items usually holds fewer items than there are CTAs
-// (the image preset: 384 items on 152 CTAs, a last wave of 80). Instead of
-// leaving the other CTAs idle, the tail items' key blocks, counted one item
-// after the other (u = (item - tail_first) * nblk + key block), are divided
-// into equal ranges of tail_len blocks, one per CTA. A CTA's range cuts items
-// into pieces [k0, k1) of their key blocks: a piece that ends inside its item
-// ("partial") writes its unnormalised O, running maximum and row sum to the
-// workspace slot of its CTA and raises a flag; the piece that holds an item's
-// last key block ("final", k0 > 0) waits for the partials of the same item -
-// they belong to the CTAs just before it - merges them into its own and
-// stores the tile as usual. tail_len <= nblk, so a range touches at most two
-// items, and at most one piece per CTA is partial (its range's last). Each CTA
-// runs its partial piece first: final pieces wait only on pieces that never
-// wait, and they are held by lower-numbered CTAs, which start no later.
-// The tail runs as a second kernel (SPLIT = true) right behind the plain one
-// (items below tail_first): the plain kernel lets it launch at once
-// (programmatic dependent launch), so each of its CTAs starts on the SM that
-// a plain CTA leaves. The tail kernel reads only q, k and v, which the plain
-// kernel does not write, so it needs no wait for the plain kernel's results;
-// keeping the tail apart leaves the plain kernel's code and registers as they
-// are.
+// ------------------------------------------------------------------ split schedule
+// Work items are pairs of 128-row query tiles with nblk key blocks each; a
+// wave holds one item per CTA. When the number of items is not a multiple of
+// the grid, the last wave leaves CTAs idle (the image preset: 384 items on
+// 152 CTAs, a last wave of 80). A split launch instead counts the key blocks
+// of items [tail_first, total) one item after the other (u = (item -
+// tail_first) * nblk + key block) and gives each CTA one range of tail_len
+// consecutive blocks. Two uses: the tail kernel behind the plain one, with
+// tail_first = the last wave's first item and tail_len <= nblk; and the whole
+// schedule in one kernel (tail_first = 0, tail_len = ceil(total * nblk /
+// grid), usually more than nblk).
+// A range cuts items into pieces [k0, k1) of their key blocks, run in the
+// range's order. A piece that starts inside its item (k0 > 0, the range's
+// first) is "partial": it writes its unnormalised O, running maximum and row
+// sum to the workspace slot of its range and raises per-warp flags. The piece
+// holding the item's first key block but not its last (k0 = 0, k1 < nblk, the
+// range's last) is "final": it waits for the flags of the ranges after its
+// own that hold the rest of the item, merges their partials into its
+// accumulator and stores the tile as usual. A range thus has at most one
+// partial piece, run first, and one final piece, run last; partial pieces
+// never wait. Range g runs on CTA grid - 1 - g, so a final piece waits only
+// for CTAs of lower index, which the hardware dispatches no later.
+// In the tail kernel (SPLIT = true, launched right behind the plain kernel
+// with programmatic dependent launch) each CTA starts on the SM that a plain
+// CTA leaves; it reads only q, k and v, which the plain kernel does not write,
+// so it needs no wait for the plain kernel's results. Keeping the split paths
+// in their own instantiation leaves the plain kernel's code and registers as
+// they are.
 struct Piece {
   int item, k0, k1;
   int kind;  // 0: a whole item; 1: partial (to the workspace); 2: final piece of a split item
 };
 
-// Tail piece k (0 or 1) of this CTA, in processing order: the range's last
-// piece first when it ends inside its item (a partial that later CTAs' final
-// pieces wait for), then the others in order. False when there is none.
+// The range this CTA runs (the split schedule's g).
+__device__ __forceinline__ int split_range() { return static_cast<int>(gridDim.x - 1 - blockIdx.x); }
+
+// Piece k (0, 1, ...) of this CTA's range, in order; false past its last.
 __device__ __forceinline__ bool tail_piece(const Params& p, int k, Piece& out) {
   const int R = (p.total - p.tail_first) * p.nblk;
-  const int u0 = static_cast<int>(blockIdx.x) * p.tail_len;
+  const int u0 = split_range() * p.tail_len;
   const int u1 = min(u0 + p.tail_len, R);
   if (u0 >= u1) return false;
-  const int i0 = u0 / p.nblk, i1 = (u1 - 1) / p.nblk;
-  const int k0_first = u0 - i0 * p.nblk;
-  const int k1_last = u1 - i1 * p.nblk;
-  if (k1_last < p.nblk) {
-    if (k == 0) {
-      out = Piece{p.tail_first + i1, i1 == i0 ? k0_first : 0, k1_last, 1};
-      return true;
-    }
-    if (i1 == i0) return false;
-    out = Piece{p.tail_first + i0, k0_first, p.nblk, k0_first > 0 ? 2 : 0};  // k == 1: the first item's end
-    return k == 1;
-  }
-  const int i = i0 + k;
-  if (i > i1) return false;
-  const int kb = i == i0 ? k0_first : 0;
-  out = Piece{p.tail_first + i, kb, p.nblk, kb > 0 ? 2 : 0};
+  const int i0 = u0 / p.nblk, i = i0 + k;
+  if (i > (u1 - 1) / p.nblk) return false;
+  const int k0 = k == 0 ? u0 - i0 * p.nblk : 0;
+  const int k1 = min(u1 - i * p.nblk, p.nblk);
+  out = Piece{p.tail_first + i, k0, k1, k0 > 0 ? 1 : (k1 < p.nblk ? 2 : 0)};
   return true;
 }
 
@@ -692,14 +689,17 @@ __device__ __forceinline__ bool bulk_store_tile(const Maps<NMAP>* maps, uint32_t
   return true;
 }
 
-// Split tail, partial piece: this thread's row of the tile - unnormalised O
-// (read from TMEM, 32 columns at a time), running maximum m (log2 domain) and
-// row sum l - into the CTA's workspace slot; then the warp's flag is raised to
-// this launch's epoch (every lane's stores fenced first).
+// Partial piece of a split item: this thread's row of the tile - unnormalised
+// O (read from TMEM, 32 columns at a time), running maximum m (log2 domain)
+// and row sum l - into the workspace slot of this CTA's range; then the warp's
+// flag is raised to this launch's epoch (every lane's stores fenced first).
+// Measured on GB300: releasing O before the stores and raising the flag a
+// piece later, after the stores had drained, made the split schedule 2 %
+// slower (image preset) than waiting for them here.
 template <int D>
 __device__ __forceinline__ void write_partial(const Params& p, int t, int r, int lane, int w4, uint32_t tO, float m,
                                               float l) {
-  const size_t tile = static_cast<size_t>(blockIdx.x) * 2 + t;
+  const size_t tile = static_cast<size_t>(split_range()) * 2 + t;
   const size_t row = tile * kBM + r;
   float4* dst = reinterpret_cast<float4*>(p.ws_o) + tile * (D / 4) * kBM + r;  // column group g at dst[g * 128]
 #pragma unroll 1
@@ -714,24 +714,25 @@ __device__ __forceinline__ void write_partial(const Params& p, int t, int r, int
   *reinterpret_cast<float2*>(p.ws_ml + row * 2) = make_float2(m, l);
   __threadfence();
   __syncwarp();
-  if (lane == 0) st_release_gpu_u32(p.ws_flags + (blockIdx.x * 2 + t) * 4 + w4, p.epoch);
+  if (lane == 0) st_release_gpu_u32(p.ws_flags + tile * 4 + w4, p.epoch);
 }
 
-// Split tail, final piece of `item`: merge the partial pieces of the same item
-// (held by CTAs c_lo .. blockIdx.x - 1, whose ranges cover its first key
+// Final piece of a split `item`: merge the partial pieces of the same item
+// (ranges g + 1 .. g_last after this CTA's g, which cover the item's other key
 // blocks) into this row's accumulator O in TMEM (tO) and its (m, l): with M
 // the largest maximum, O = sum O_i 2^(m_i - M) and l = sum l_i 2^(m_i - M)
 // over the pieces, the usual combination of softmax partial results. One
-// partial at a time, 32 columns at a time, so that it needs few registers.
+// partial at a time, 32 columns at a time, so that it needs few registers
+// (loading the next 32 columns meanwhile measured no faster).
 // Each warp waits only for the same warp of the other CTAs (it holds the same
 // rows). Called before O is released to the next piece. False on abort.
 template <int D>
 __device__ __forceinline__ bool merge_partials(const Params& p, int item, int t, int r, int w4, uint32_t tO, float& m,
                                                float& l, const WaitCtl& w) {
-  const int U = (item - p.tail_first) * p.nblk;
-  for (int cs = U / p.tail_len; cs < static_cast<int>(blockIdx.x); ++cs) {
-    if (!__all_sync(0xffffffffu, flag_wait(p.ws_flags + (cs * 2 + t) * 4 + w4, p.epoch, w))) return false;
-    const size_t tile = static_cast<size_t>(cs) * 2 + t;
+  const int g_last = ((item - p.tail_first) * p.nblk + p.nblk - 1) / p.tail_len;
+  for (int gs = split_range() + 1; gs <= g_last; ++gs) {
+    const size_t tile = static_cast<size_t>(gs) * 2 + t;
+    if (!__all_sync(0xffffffffu, flag_wait(p.ws_flags + tile * 4 + w4, p.epoch, w))) return false;
     const size_t row = tile * kBM + r;
     const float2 ml = *reinterpret_cast<const float2*>(p.ws_ml + row * 2);
     const float mx = fmaxf(m, ml.x);
@@ -743,11 +744,11 @@ __device__ __forceinline__ bool merge_partials(const Params& p, int item, int t,
       tmem_ld_x32(tO + c * 32, x);
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const float4 y = src[(c * 8 + i) * kBM];
-        x[4 * i + 0] = __float_as_uint(fmaf(__uint_as_float(x[4 * i + 0]), a, y.x * b));
-        x[4 * i + 1] = __float_as_uint(fmaf(__uint_as_float(x[4 * i + 1]), a, y.y * b));
-        x[4 * i + 2] = __float_as_uint(fmaf(__uint_as_float(x[4 * i + 2]), a, y.z * b));
-        x[4 * i + 3] = __float_as_uint(fmaf(__uint_as_float(x[4 * i + 3]), a, y.w * b));
+        const float4 yy = src[(c * 8 + i) * kBM];
+        x[4 * i + 0] = __float_as_uint(fmaf(__uint_as_float(x[4 * i + 0]), a, yy.x * b));
+        x[4 * i + 1] = __float_as_uint(fmaf(__uint_as_float(x[4 * i + 1]), a, yy.y * b));
+        x[4 * i + 2] = __float_as_uint(fmaf(__uint_as_float(x[4 * i + 2]), a, yy.z * b));
+        x[4 * i + 3] = __float_as_uint(fmaf(__uint_as_float(x[4 * i + 3]), a, yy.w * b));
       }
       tmem_st_x32(tO + c * 32, x);
     }

@@ -10,7 +10,7 @@
 namespace attn_a2a {
 
 template <int D, int MODE, int NMAP, bool TRACE = false, bool SPLIT = false>
-int launch_t(const tc::Maps<NMAP>& maps, const tc::Params& p, int grid, cudaStream_t stream) {
+int launch_t(const tc::Maps<NMAP>& maps, const tc::Params& p, int grid, cudaStream_t stream, bool pdl = false) {
   auto kern = tc::fa_fwd_tc_kernel<D, MODE, NMAP, TRACE, SPLIT>;
   constexpr int smem = tc::kBulkStores<MODE> ? tc::Cfg<D>::SMEM_ALLOC_STG : tc::Cfg<D>::SMEM_ALLOC;
   // The in-kernel register split assumes exactly this launch register count;
@@ -21,7 +21,7 @@ int launch_t(const tc::Maps<NMAP>& maps, const tc::Params& p, int grid, cudaStre
   if (attr.numRegs != tc::kLaunchRegs) return ATTN_A2A_EUNSUPPORTED;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return ATTN_A2A_ECUDA;
-  if constexpr (SPLIT) {
+  if (pdl) {
     // the tail kernel, queued behind the plain one: launched with programmatic
     // stream serialisation, so its CTAs start as the plain kernel's CTAs exit
     cudaLaunchConfig_t cfg = {};
@@ -39,10 +39,9 @@ int launch_t(const tc::Maps<NMAP>& maps, const tc::Params& p, int grid, cudaStre
       return ATTN_A2A_ECUDA;
     }
     return ATTN_A2A_OK;
-  } else {
-    kern<<<grid, tc::kThreads, smem, stream>>>(maps, p);
-    return cudaGetLastError() == cudaSuccess ? ATTN_A2A_OK : ATTN_A2A_ECUDA;
   }
+  kern<<<grid, tc::kThreads, smem, stream>>>(maps, p);
+  return cudaGetLastError() == cudaSuccess ? ATTN_A2A_OK : ATTN_A2A_ECUDA;
 }
 
 // The traced instantiations (per-tile stamps into p.trace) of the four
@@ -50,10 +49,11 @@ int launch_t(const tc::Maps<NMAP>& maps, const tc::Params& p, int grid, cudaStre
 int launch_fa_tc_traced(const tc::Maps<1>& maps, const tc::Params& p, int d, int mode, int grid,
                         cudaStream_t stream);
 
-// The tail kernel of a split tail (pieces of items tail_first .. total - 1,
-// workspace in p) of the same four modes, launched behind the plain kernel
-// that runs items 0 .. tail_first - 1.
+// The split instantiation (pieces of items tail_first .. total - 1, workspace
+// in p) of the same four modes: with pdl, the tail kernel launched behind the
+// plain kernel that runs items 0 .. tail_first - 1; without, the whole
+// schedule on its own.
 int launch_fa_tc_split(const tc::Maps<1>& maps, const tc::Params& p, int d, int mode, int grid,
-                       cudaStream_t stream);
+                       cudaStream_t stream, bool pdl);
 
 }  // namespace attn_a2a

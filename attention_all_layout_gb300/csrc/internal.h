@@ -15,6 +15,8 @@ struct Problem {
 };
 
 int num_sms_current_device();
+// L2 cache bytes of the current device (0 if unknown).
+long long l2_bytes_current_device();
 
 // The epilogue's store kind for a request: 1 = bulk tensor stores, 2 = row
 // stores, or 0 when store_kind 1 asks for bulk stores where they are not

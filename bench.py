@@ -43,13 +43,29 @@ KERNEL_SOURCES = ["fa_tc.cuh", "ptx.cuh", "epilogue.cuh", "tmem_ops.cuh", "fa_tc
                   "fa_tc_split.cu"]
 
 
-def split_tail_used(cfg, grid: int) -> bool:
-    """Whether a call with a workspace splits its last wave: fewer items than CTAs in it."""
-    npair = ((cfg.S + 127) // 128 + 1) // 2
-    total = cfg.B * cfg.H * npair
+def split_plan(cfg, grid: int, l2_bytes: int):
+    """How a call with a workspace and the automatic split divides cfg's work items (the
+    launcher's rule): "all" (every item's key blocks in equal ranges, one kernel), "tail"
+    (the partial last wave's, in a second kernel) or None."""
+    nblk = (cfg.S + 127) // 128
+    total = cfg.B * cfg.H * ((nblk + 1) // 2)
     grid = min(grid, total)
+    if nblk < 2:
+        return None
     waves = (total + grid - 1) // grid
-    return total - (waves - 1) * grid < grid and (cfg.S + 127) // 128 >= 2
+    if 2 * 4 * cfg.B * cfg.H * cfg.S * cfg.d <= l2_bytes and waves * nblk - (total * nblk + grid - 1) // grid >= 4:
+        return "all"
+    r = total - (waves - 1) * grid
+    if r < grid and nblk - (r * nblk + grid - 1) // grid >= 32:
+        return "tail"
+    return None
+
+
+def device_split_plan(cfg):
+    import torch
+    from attention_all_layout_gb300 import binding as bd
+
+    return split_plan(cfg, bd.num_sms(), torch.cuda.get_device_properties(0).L2_cache_size)
 
 
 def fused_kernel_label(cfg, split: bool) -> str:
@@ -57,10 +73,10 @@ def fused_kernel_label(cfg, split: bool) -> str:
     from attention_all_layout_gb300 import binding as bd
 
     bulk = bd.attn_a2a_store_kind(cfg.S, cfg.P, 1) == 1
-    split = split and split_tail_used(cfg, bd.num_sms())
-    return (f"fa_fwd_tc_kernel<{cfg.d}, {3 if bulk else 1}, 1, false, {'true' if split else 'false'}> "
-            f"(all-to-all layout, {'bulk-store' if bulk else 'row-store'} epilogue"
-            f"{', split tail' if split else ''})")
+    plan = device_split_plan(cfg) if split else None
+    what = {"tail": ", split tail", "all": ", whole schedule split", None: ""}[plan]
+    return (f"fa_fwd_tc_kernel<{cfg.d}, {3 if bulk else 1}, 1, false, {'true' if plan else 'false'}> "
+            f"(all-to-all layout, {'bulk-store' if bulk else 'row-store'} epilogue{what})")
 
 
 def dist_env():
@@ -377,7 +393,8 @@ def main():
             print(json.dumps({"metric": METRIC, "value": cfg.flops / (ms * 1e-3) / 1e12 * world,
                               "unit": "TFLOP/s", "ms_per_step": ms, "steps": args.steps,
                               "config": {"workload": cfg.name, "B": cfg.B, "H": cfg.H, "S": cfg.S,
-                                         "d": cfg.d, "P": cfg.P, "split_tail": ws is not None},
+                                         "d": cfg.d, "P": cfg.P,
+                                         "split": device_split_plan(cfg) if ws is not None else None},
                               "clocks": clocks, "fused_only": True}),
                   flush=True)
         return 0
@@ -490,7 +507,7 @@ def main():
                    "S": cfg.S, "d": cfg.d, "P": cfg.P,
                    "l2": "no flush: q,k,v inputs (%.2f GB) exceed the 129 MB L2" % (cfg.qkv_bytes / 1e9),
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU, P virtual ranks",
-                   "split_tail": ws is not None},
+                   "split": device_split_plan(cfg) if ws is not None else None},
         "pct_of_bf16_peak": 100.0 * tflops / peak,
         "pct_of_bf16_peak_sustained": 100.0 * tflops / peaks.get("bf16_tflops_sustained", peak),
         "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
@@ -510,7 +527,7 @@ def main():
                 "ms_per_step": ms_e2e},
         "clocks": clocks,
         # the split tail runs as a second kernel behind the first one
-        "gpu_launches": args.steps * (2 if ws is not None and split_tail_used(cfg, bd.num_sms()) else 1),
+        "gpu_launches": args.steps * (2 if ws is not None and device_split_plan(cfg) == "tail" else 1),
         "cpu_baseline": cpu,
         "other_presets_fused": presets or None,
     }

@@ -131,20 +131,29 @@ typedef struct {
                            address space, this is the one-sided store of the pages'
                            FlashAttention-A2A ("Key Contributions") from rank r's tile
                            owners into rank j's buffer */
-  int reserved;
+  int split;            /* 0 in normal use. With a workspace, how work items are divided
+                           by key blocks (see workspace): ATTN_A2A_SPLIT_AUTO (0) lets
+                           the library choose; ATTN_A2A_SPLIT_TAIL (1) divides only a
+                           partial last wave, whenever there is one; ATTN_A2A_SPLIT_ALL
+                           (2) divides every item's key blocks into equal ranges, one
+                           per CTA, in one kernel; ATTN_A2A_SPLIT_NONE (3) divides
+                           nothing. Other values: ATTN_A2A_EINVAL */
   void* workspace;      /* NULL in normal use. Device scratch of at least
                            ATTN_A2A_WORKSPACE_BYTES(grid, d) bytes (grid = the
                            persistent CTAs, attn_a2a_num_sms() by default), 256-byte
                            aligned, zeroed by the caller before its first use, not
                            overlapping any input or output. With it, when the last wave
-                           of work items holds fewer items than there are CTAs and
-                           dividing it saves each CTA at least 32 key blocks (long
-                           sequences), that wave's key blocks are divided over all CTAs
-                           in a second kernel queued behind the first (programmatic
-                           dependent launch): a CTA whose range ends inside an item
-                           writes that item's partial result here; the CTA holding the
-                           item's last key block merges the partials and stores the tile.
-                           Otherwise the call is the same as without a workspace. The
+                           of work items holds fewer items than there are CTAs, key
+                           blocks of items are divided into equal ranges, one per CTA
+                           (the split option): either the last wave's, in a second
+                           kernel queued behind the first (programmatic dependent
+                           launch), or every item's, in one kernel. A range that starts
+                           inside an item writes that piece's partial result here; the
+                           range holding the item's first key block merges the partials
+                           and stores the tile. The automatic choice divides the last
+                           wave when that saves each CTA at least 32 key blocks (long
+                           sequences). Otherwise the call is the same as without a
+                           workspace. The
                            kernel leaves the workspace valid for the next call; calls
                            that share one workspace must not run at the same time. Not
                            used with tile_order = 1 or trace. The split items agree with
@@ -153,6 +162,12 @@ typedef struct {
                            attn_a2a_fwd_ex and attn_a2a_fwd_contig_ex only */
   long long workspace_bytes; /* size of workspace */
 } attn_a2a_opts;
+
+/* attn_a2a_opts.split */
+#define ATTN_A2A_SPLIT_AUTO 0
+#define ATTN_A2A_SPLIT_TAIL 1
+#define ATTN_A2A_SPLIT_ALL 2
+#define ATTN_A2A_SPLIT_NONE 3
 
 /* Workspace bytes of attn_a2a_opts.workspace for a grid of `grid` CTAs and
  * head dimension d: per CTA, a flag word per (query tile, warp), and one

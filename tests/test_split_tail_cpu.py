@@ -1,118 +1,153 @@
-"""CPU test of the split-tail work decomposition of the attention kernel
-(plan_split_tail on the host, tail_piece / piece_at / merge_partials' CTA
-range on the device), restated here in Python and checked for the properties
-the kernel relies on, over many (items, grid, key blocks) geometries:
+"""CPU test of the split work decomposition of the attention kernel
+(plan_split_tail on the host, tail_piece / piece_at / merge_partials' range of
+ranges on the device), restated here in Python and checked for the properties
+the kernel relies on, over many (items, grid, key blocks) geometries and both
+split kinds (the last wave in a tail kernel; every item in one kernel):
 
 * every (item, key block) of the problem is computed exactly once;
-* each CTA gets at most two tail pieces, and at most one of them is partial,
-  processed first;
-* every split item has exactly one final piece (it holds the item's last key
-  block), and the CTAs the merge reads from are exactly the ones holding its
-  partial pieces - so a final piece only waits on pieces that wait on nothing;
-* the CTA ranges balance the tail: no CTA holds more than tail_len blocks;
-* the launcher splits only when that saves at least 32 key blocks per CTA
-  (the image and joint presets keep the unsplit schedule, video and long split).
+* a range holds at most tail_len blocks, at most one partial piece (its first)
+  and at most one final piece (its last);
+* every split item has exactly one final piece, the one holding its first key
+  block; the ranges its merge reads are exactly those holding the item's other
+  blocks, each of which holds exactly one partial piece, of this item, and
+  runs on a CTA of lower index than the final piece's - so a final piece waits
+  only on pieces that wait on nothing, on CTAs dispatched no later;
+* the automatic choice takes the whole-schedule split where the K and V of
+  every head fit in half of L2 and it saves at least 4 key blocks per CTA (the
+  image and joint presets), else the last wave's split where that saves at
+  least 32 key blocks per CTA (video and long).
 """
 import pytest
 
+AUTO, TAIL, ALL, NONE = 0, 1, 2, 3
 
-def plan(total, grid, nblk, min_saved=32):
+
+L2 = 126 * 2**20  # an L2 of GB300 size, for the automatic choice
+
+
+def plan(total, grid, nblk, split=AUTO, min_saved=32, kv_bytes=1 << 40, l2=L2):
+    """(tail_first, tail_len, whole) as the host launcher computes them; kv_bytes =
+    the K and V bytes of every head (4 * B * H * S * d)."""
+    if split == NONE or nblk < 2:
+        return total, 0, False
     waves = (total + grid - 1) // grid
+    all_len = (total * nblk + grid - 1) // grid
+    if split == ALL or (split == AUTO and 2 * kv_bytes <= l2 and waves * nblk - all_len >= 4):
+        return 0, all_len, True
     r = total - (waves - 1) * grid
-    if r >= grid or nblk < 2:
-        return total, 0
+    if r >= grid:
+        return total, 0, False
     length = (r * nblk + grid - 1) // grid
-    if nblk - length < min_saved:
-        return total, 0
-    return (waves - 1) * grid, length
+    if split == AUTO and nblk - length < min_saved:
+        return total, 0, False
+    return (waves - 1) * grid, length, False
 
 
-def tail_piece(total, tail_first, tail_len, nblk, cta, k):
+def tail_piece(total, tail_first, tail_len, nblk, grid, cta, k):
+    """Piece k of CTA cta's range (range g = grid - 1 - cta), or None."""
+    g = grid - 1 - cta
     R = (total - tail_first) * nblk
-    u0 = cta * tail_len
+    u0 = g * tail_len
     u1 = min(u0 + tail_len, R)
     if u0 >= u1:
         return None
-    i0, i1 = u0 // nblk, (u1 - 1) // nblk
-    k0_first = u0 - i0 * nblk
-    k1_last = u1 - i1 * nblk
-    if k1_last < nblk:
-        if k == 0:
-            return (tail_first + i1, k0_first if i1 == i0 else 0, k1_last, 1)
-        if i1 == i0 or k != 1:
-            return None
-        return (tail_first + i0, k0_first, nblk, 2 if k0_first > 0 else 0)
+    i0 = u0 // nblk
     i = i0 + k
-    if i > i1:
+    if i > (u1 - 1) // nblk:
         return None
-    kb = k0_first if i == i0 else 0
-    return (tail_first + i, kb, nblk, 2 if kb > 0 else 0)
+    k0 = u0 - i0 * nblk if k == 0 else 0
+    k1 = min(u1 - i * nblk, nblk)
+    kind = 1 if k0 > 0 else (2 if k1 < nblk else 0)
+    return (tail_first + i, k0, k1, kind)
 
 
-def pieces(total, grid, nblk, cta, min_saved=0):
-    tail_first, tail_len = plan(total, grid, nblk, min_saved)
-    main_end = min(tail_first, total)
-    out = [(item, 0, nblk, 0) for item in range(cta, main_end, grid)]
-    if tail_first < total:
-        for k in range(3):
-            pc = tail_piece(total, tail_first, tail_len, nblk, cta, k)
-            if pc is None:
-                break
-            out.append(pc)
-    return out, tail_first, tail_len
+def merge_ranges(item, tail_first, tail_len, nblk, grid, cta):
+    """The ranges merge_partials reads for the final piece of `item` on CTA cta."""
+    g = grid - 1 - cta
+    g_last = ((item - tail_first) * nblk + nblk - 1) // tail_len
+    return list(range(g + 1, g_last + 1))
+
+
+def schedule(total, grid, nblk, split):
+    tail_first, tail_len, whole = plan(total, grid, nblk, split)
+    per_cta = []
+    for cta in range(grid):
+        out = [] if whole else [(item, 0, nblk, 0) for item in range(cta, min(tail_first, total), grid)]
+        split_pcs = []
+        if tail_first < total:
+            k = 0
+            while (pc := tail_piece(total, tail_first, tail_len, nblk, grid, cta, k)) is not None:
+                split_pcs.append(pc)
+                k += 1
+        per_cta.append((out, split_pcs))
+    return tail_first, tail_len, whole, per_cta
 
 
 GEOMS = [(total, grid, nblk) for total in (1, 2, 5, 20, 23, 152, 153, 384, 432, 5120)
          for grid in (1, 3, 7, 16, 152) for nblk in (1, 2, 3, 8, 32, 36, 256) if grid <= max(total, 1)]
 
 
+@pytest.mark.parametrize("split", [TAIL, ALL])
 @pytest.mark.parametrize("total,grid,nblk", GEOMS)
-def test_split_tail_plan(total, grid, nblk):
+def test_split_plan(total, grid, nblk, split):
     grid = min(grid, total)
+    tail_first, tail_len, whole, per_cta = schedule(total, grid, nblk, split)
     covered = {}
-    per_cta = []
-    tail_first = tail_len = None
-    for cta in range(grid):
-        pcs, tail_first, tail_len = pieces(total, grid, nblk, cta)
-        per_cta.append(pcs)
-        tail = [pc for pc in pcs if pc[0] >= tail_first]
-        assert len(tail) <= 2
-        partial = [i for i, pc in enumerate(tail) if pc[3] == 1]
-        assert partial in ([], [0])  # a partial piece comes first
-        assert sum(pc[2] - pc[1] for pc in tail) <= max(tail_len, nblk if tail_first >= total else tail_len)
-        for item, k0, k1, kind in pcs:
+    for cta, (plain, pcs) in enumerate(per_cta):
+        if pcs:
+            assert sum(k1 - k0 for _, k0, k1, _ in pcs) <= tail_len
+        kinds = [pc[3] for pc in pcs]
+        assert kinds.count(1) <= 1 and (1 not in kinds or kinds[0] == 1)  # a partial piece comes first
+        assert kinds.count(2) <= 1 and (2 not in kinds or kinds[-1] == 2)  # a final piece comes last
+        for item, k0, k1, kind in plain + pcs:
             assert 0 <= k0 < k1 <= nblk
-            assert (kind == 1) == (k1 < nblk) and (kind == 2) == (k1 == nblk and k0 > 0)
+            assert (kind == 1) == (k0 > 0) and (kind == 2) == (k0 == 0 and k1 < nblk)
             for j in range(k0, k1):
                 assert (item, j) not in covered
                 covered[(item, j)] = cta
     assert len(covered) == total * nblk
-    if tail_first < total:
-        assert 1 <= tail_len <= nblk
-        for item in range(tail_first, total):
-            finals = [(c, pc) for c, pcs in enumerate(per_cta) for pc in pcs if pc[0] == item and pc[2] == nblk]
-            assert len(finals) == 1
-            c, (_, kb, _, kind) = finals[0]
-            holders = sorted({covered[(item, j)] for j in range(kb)})
-            if kind == 2:
-                U = (item - tail_first) * nblk
-                assert holders == list(range(U // tail_len, c))  # merge_partials' CTA range
-                for h in holders:  # each holds exactly one partial piece: of this item
-                    assert [pc for pc in per_cta[h] if pc[3] == 1] == [pc for pc in per_cta[h] if pc[0] == item]
-            else:
-                assert holders in ([], [c])
+    if tail_first >= total:
+        return
+    assert tail_len >= 1 and (whole or tail_len <= nblk)
+    for item in range(tail_first, total):
+        holders = {covered[(item, j)] for j in range(nblk)}
+        finals = [(c, pc) for c, (_, pcs) in enumerate(per_cta) for pc in pcs if pc[0] == item and pc[3] == 2]
+        if len(holders) == 1:
+            assert finals == []  # a whole item
+            continue
+        assert len(finals) == 1
+        c, (_, k0, k1, _) = finals[0]
+        assert k0 == 0
+        others = sorted({covered[(item, j)] for j in range(k1, nblk)})
+        read = [grid - 1 - g for g in merge_ranges(item, tail_first, tail_len, nblk, grid, c)]
+        assert sorted(read) == others
+        for h in others:
+            assert h < c  # dispatched no later than the waiting CTA
+            assert [pc for pc in per_cta[h][1] if pc[3] == 1] == [pc for pc in per_cta[h][1] if pc[0] == item]
 
 
-def test_tail_shapes_of_the_presets():
+def kv(B, H, S, d):
+    return 4 * B * H * S * d
+
+
+def test_split_shapes_of_the_presets():
     # image: 384 items of 32 key blocks on 152 CTAs -> a last wave of 80 items; 17-block
-    # ranges would save only 15 blocks per CTA, so the tail is not split
-    assert plan(384, 152, 32, min_saved=0) == (304, 17)
-    assert plan(384, 152, 32) == (384, 0)
-    # joint: 432 items of 36 blocks -> 128 in the last wave, 31-block ranges: not split
-    assert plan(432, 152, 36) == (432, 0)
-    # video: 5120 items of 256 blocks -> 104 in the last wave, 176-block ranges (80 saved)
-    assert plan(5120, 152, 256) == (5016, 176)
+    # tail ranges would save only 15 blocks per CTA, the whole schedule in 81-block
+    # ranges saves 15 of 96, and K and V (50 MB) fit in half of L2: the whole schedule
+    image = kv(1, 24, 4096, 128)
+    assert plan(384, 152, 32, TAIL) == (304, 17, False)
+    assert plan(384, 152, 32, kv_bytes=image) == (0, 81, True)
+    assert plan(384, 152, 32, ALL) == (0, 81, True)
+    assert plan(384, 152, 32, kv_bytes=image, l2=64 * 2**20) == (384, 0, False)  # a smaller L2: no split
+    # joint: 432 items of 36 blocks -> 128 in the last wave; 103-block ranges save 5 of 108
+    assert plan(432, 152, 36, kv_bytes=kv(1, 24, 4608, 128)) == (0, 103, True)
+    assert plan(432, 152, 36) == (432, 0, False)  # K and V beyond half of L2: no split
+    # video: 5120 items of 256 blocks -> 104 in the last wave, 176-block ranges (80 saved);
+    # K and V (671 MB) far beyond L2
+    assert plan(5120, 152, 256, kv_bytes=kv(1, 40, 32768, 128)) == (5016, 176, False)
     # long: 11840 items of 591 blocks -> 136 in the last wave, 529-block ranges (62 saved)
-    assert plan(11840, 152, 591) == (11704, 529)
-    # a full last wave is not split
-    assert plan(304, 152, 32) == (304, 0)
+    assert plan(11840, 152, 591, kv_bytes=kv(1, 40, 75600, 128)) == (11704, 529, False)
+    # a full last wave is not split by the tail kinds
+    assert plan(304, 152, 32) == (304, 0, False)
+    assert plan(304, 152, 32, TAIL) == (304, 0, False)
+    assert plan(304, 152, 32, NONE) == (304, 0, False)

@@ -368,7 +368,8 @@ def attn_a2a_num_sms() -> int:
 
 
 def attn_a2a_store_kind(S: int, P: int, layout: int, store_kind: int = 0) -> int:
-    """Store kind the library uses for these sizes: 1 = bulk tensor stores, 2 = row stores.
+    """Store kind the library uses for these sizes: 1 = bulk tensor stores, 2 = row stores,
+    3 = whole-line row stores (all-to-all layout, on request only).
     layout 0 = contiguous (attention alone), 1 = all-to-all. Raises AttnA2AError on a bad request."""
     out = ctypes.c_int(0)
     rc = load().attn_a2a_store_kind(int(S), int(P), int(layout), int(store_kind), ctypes.byref(out))

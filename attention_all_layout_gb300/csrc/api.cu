@@ -189,7 +189,7 @@ int fwd_common(const void* q, const void* k, const void* v, const attn_a2a_shape
   bool empty = false;
   int rc = check_inputs(q, k, v, shp, scale, &empty);
   if (rc != ATTN_A2A_OK) return rc;
-  if (opts != nullptr && (opts->store_kind < 0 || opts->store_kind > 2 || opts->grid < 0 ||
+  if (opts != nullptr && (opts->store_kind < 0 || opts->store_kind > 3 || opts->grid < 0 ||
                           opts->timeout_ns < 0 || opts->inject_stall < 0 || opts->inject_stall > 1 ||
                           opts->tile_order < 0 || opts->tile_order > 1 ||
                           (reinterpret_cast<uintptr_t>(opts->trace) & 7u) != 0 || opts->part_heads < 0 ||
@@ -272,7 +272,7 @@ int attn_a2a_num_sms(void) { return num_sms_current_device(); }
 
 int attn_a2a_store_kind(int S, int P, int layout, int store_kind, int* resolved) {
   if (resolved == nullptr || S < 0 || P < 1 || P > kMaxRanks || layout < 0 || layout > 1 || store_kind < 0 ||
-      store_kind > 2)
+      store_kind > 3)
     return ATTN_A2A_EINVAL;
   const int kind = resolve_store_kind(S, P, layout == 1, store_kind);
   if (kind == 0) return ATTN_A2A_EUNSUPPORTED;

@@ -28,11 +28,13 @@ constexpr int kBulkA2AMaxBlocks = 128;
 // the contiguous layout, and the all-to-all layout with up to kMaxStoreMaps
 // partitions and at most kBulkA2AMaxBlocks key blocks (at longer sequences its
 // strided tile stores measured slower than row stores) - else row stores;
-// 1: bulk stores, or 0 where they are not built; 2: row stores.
+// 1: bulk stores, or 0 where they are not built; 2: row stores; 3: row stores
+// written as whole lines through shared memory (all-to-all layout only, else 0).
 int resolve_store_kind(int S, int P, bool a2a, int store_kind) {
   const bool built = !a2a || P <= tc::kMaxStoreMaps;
   if (store_kind == 1) return built ? 1 : 0;
   if (store_kind == 2) return 2;
+  if (store_kind == 3) return a2a ? 3 : 0;
   const bool faster = !a2a || (S + tc::kBM - 1) / tc::kBM <= kBulkA2AMaxBlocks;
   return built && faster ? 1 : 2;
 }
@@ -235,7 +237,8 @@ int launch_fa_tc(const void* q, const void* k, const void* v, const attn_a2a_sha
   bool whole = false;
   const int split_rc = plan_split_tail(p, grid, shp.d, opts, whole);
   if (split_rc != ATTN_A2A_OK) return split_rc;
-  const int mode = a2a ? (bulk ? tc::kModeA2AT : tc::kModeA2A) : (bulk ? tc::kModeContigT : tc::kModeContig);
+  const int mode = a2a ? (bulk ? tc::kModeA2AT : kind == 3 ? tc::kModeA2AC : tc::kModeA2A)
+                       : (bulk ? tc::kModeContigT : tc::kModeContig);
   if (opts.trace != nullptr) {
     p.trace = opts.trace;
     return launch_fa_tc_traced(maps, p, shp.d, mode, grid, stream);
@@ -264,6 +267,9 @@ int launch_plain(const tc::Maps<1>& maps, const tc::Params& p, int d, int mode, 
     case tc::kModeA2A:
       return d == 128 ? launch_t<128, tc::kModeA2A, 1>(maps, p, grid, stream)
                       : launch_t<64, tc::kModeA2A, 1>(maps, p, grid, stream);
+    case tc::kModeA2AC:
+      return d == 128 ? launch_t<128, tc::kModeA2AC, 1>(maps, p, grid, stream)
+                      : launch_t<64, tc::kModeA2AC, 1>(maps, p, grid, stream);
     default:
       return d == 128 ? launch_t<128, tc::kModeContig, 1>(maps, p, grid, stream)
                       : launch_t<64, tc::kModeContig, 1>(maps, p, grid, stream);

@@ -135,6 +135,13 @@ struct Cfg {
 //                no block is half empty and the result equals kModeA2A's bit
 //                for bit. Output as kModeA2A (row stores).
 //   kModeS2SGT   as kModeS2SG, with kModeA2AT's bulk-store epilogue.
+//   kModeA2AC    as kModeA2A, but each warp writes its 32 rows as whole lines:
+//                it puts 16 rows at a time into its own slice of the staging
+//                buffer, then every store instruction of the warp covers whole
+//                rows (2 of 256 bytes, or 4 of 128), so a destination reached
+//                over a slower link (another device's or the host's memory)
+//                receives full lines instead of 16-byte pieces of 32 rows.
+//                No barrier with other warps: each warp's slice is its own.
 // (kModeS2S keeps the row stores: with the staging path its register
 // pressure grew and the whole layer measured ≈ 3 % slower.)
 enum : int {
@@ -144,10 +151,14 @@ enum : int {
   kModeA2AT = 3,
   kModeContigT = 4,
   kModeS2SG = 5,
-  kModeS2SGT = 6
+  kModeS2SGT = 6,
+  kModeA2AC = 7
 };
 template <int MODE>
 constexpr bool kBulkStores = MODE == kModeA2AT || MODE == kModeContigT || MODE == kModeS2SGT;
+// modes that use the staging buffer (bulk tensor stores, or whole-line row stores)
+template <int MODE>
+constexpr bool kStagedStores = kBulkStores<MODE> || MODE == kModeA2AC;
 template <int MODE>
 constexpr bool kSegLoads = MODE == kModeS2SG || MODE == kModeS2SGT;
 constexpr int kMaxS2SRanks = 8;
@@ -758,6 +769,52 @@ __device__ __forceinline__ bool merge_partials(const Params& p, int item, int t,
   return true;
 }
 
+// kModeA2AC epilogue of one warp: its 32 rows (this lane's row in o, scaled
+// by inv_l, going to dst, or nowhere when dst is null) in two passes of 16
+// rows through the warp's own slice `wbuf` of the staging buffer (TILE_BYTES/8
+// bytes: 16 rows). Each row is written into the slice with its 16-byte chunks
+// rotated by the row index (chunk c at c ^ row, so that the 16 rows' stores
+// spread over the banks), then read back so that the lanes of one store
+// instruction hold consecutive chunks of whole rows: 512 bytes of
+// consecutive addresses per row pair (d = 128) or row quadruple (d = 64).
+template <int D>
+__device__ __forceinline__ void line_store_rows(uint32_t wbuf, int lane, uint16_t* dst, const uint32_t (&o)[D],
+                                                float inv_l) {
+  constexpr int RB = D * 2;        // bytes per row
+  constexpr int CH = RB / 16;      // 16-byte chunks per row
+  constexpr int RP = 16;           // rows per pass: the slice holds 16 rows
+  constexpr int RPI = 512 / RB;    // rows per store instruction
+  static_assert(RP * RB == Cfg<D>::TILE_BYTES / 8, "slice size");
+  const unsigned long long mine = reinterpret_cast<unsigned long long>(dst);
+#pragma unroll
+  for (int pass = 0; pass < 32 / RP; ++pass) {
+    const int rr = lane - pass * RP;  // this lane's row within the pass, if it is in it
+    if (rr >= 0 && rr < RP) {
+#pragma unroll
+      for (int c = 0; c < CH; ++c) {
+        const uint32_t x = pack_bf16x2(__uint_as_float(o[8 * c + 0]) * inv_l, __uint_as_float(o[8 * c + 1]) * inv_l);
+        const uint32_t y = pack_bf16x2(__uint_as_float(o[8 * c + 2]) * inv_l, __uint_as_float(o[8 * c + 3]) * inv_l);
+        const uint32_t z = pack_bf16x2(__uint_as_float(o[8 * c + 4]) * inv_l, __uint_as_float(o[8 * c + 5]) * inv_l);
+        const uint32_t w = pack_bf16x2(__uint_as_float(o[8 * c + 6]) * inv_l, __uint_as_float(o[8 * c + 7]) * inv_l);
+        const uint32_t a = wbuf + static_cast<uint32_t>(rr * RB + ((c ^ (rr & (CH - 1))) * 16));
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
+      }
+    }
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < RP / RPI; ++i) {
+      const int row = i * RPI + lane / CH;  // within the pass
+      const int c = lane % CH;
+      const unsigned long long rp = __shfl_sync(0xffffffffu, mine, pass * RP + row);
+      const uint32_t a = wbuf + static_cast<uint32_t>(row * RB + ((c ^ (row & (CH - 1))) * 16));
+      uint4 v;
+      asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+      if (rp != 0ull) reinterpret_cast<uint4*>(rp)[c] = v;
+    }
+    __syncwarp();
+  }
+}
+
 template <int D, int MODE, int NMAP, bool TRACE, bool SPLIT>
 __device__ void softmax_role(const Params& p, int t, uint32_t bar0, uint32_t tmem, const Maps<NMAP>* maps,
                              uint32_t stg, const WaitCtl& w) {
@@ -946,7 +1003,7 @@ __device__ void softmax_role(const Params& p, int t, uint32_t bar0, uint32_t tme
                 ((static_cast<int64_t>(wi.b) * bq.c + lrow) * p.H + wi.h) * D;
       }
     } else if (srow < p.S) {
-      if constexpr (MODE == kModeA2A) {
+      if constexpr (MODE == kModeA2A || MODE == kModeA2AC) {
         if (p.epi.crem == 0) {
           // equal partitions: the row's partition is one division away
           // (measured 0.3 % faster per launch at the video shape than the
@@ -962,7 +1019,10 @@ __device__ void softmax_role(const Params& p, int t, uint32_t bar0, uint32_t tme
         dst = out_row_ptr<D, MODE != kModeContig && MODE != kModeContigT>(p.epi, p.B, p.H, p.S, wi.b, wi.h, srow);
       }
     }
-    if (dst != nullptr) {
+    if constexpr (MODE == kModeA2AC) {
+      line_store_rows<D>(stg + static_cast<uint32_t>(t * 4 + (warp & 3)) * (Cfg<D>::TILE_BYTES / 8), lane, dst, o,
+                         1.0f / l);
+    } else if (dst != nullptr) {
       const float inv_l = 1.0f / l;
       uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll

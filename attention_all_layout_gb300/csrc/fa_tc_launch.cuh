@@ -12,7 +12,7 @@ namespace attn_a2a {
 template <int D, int MODE, int NMAP, bool TRACE = false, bool SPLIT = false>
 int launch_t(const tc::Maps<NMAP>& maps, const tc::Params& p, int grid, cudaStream_t stream, bool pdl = false) {
   auto kern = tc::fa_fwd_tc_kernel<D, MODE, NMAP, TRACE, SPLIT>;
-  constexpr int smem = tc::kBulkStores<MODE> ? tc::Cfg<D>::SMEM_ALLOC_STG : tc::Cfg<D>::SMEM_ALLOC;
+  constexpr int smem = tc::kStagedStores<MODE> ? tc::Cfg<D>::SMEM_ALLOC_STG : tc::Cfg<D>::SMEM_ALLOC;
   // The in-kernel register split assumes exactly this launch register count;
   // with fewer registers at launch the softmax warpgroups could never obtain
   // their share, so refuse to launch rather than risk a stuck kernel.

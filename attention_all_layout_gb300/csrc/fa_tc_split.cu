@@ -17,6 +17,7 @@ int launch_fa_tc_split(const tc::Maps<1>& maps, const tc::Params& p, int d, int 
       case tc::kModeA2A: return launch_t<128, tc::kModeA2A, 1, false, true>(maps, p, grid, stream, pdl);
       case tc::kModeA2AT: return launch_t<128, tc::kModeA2AT, 1, false, true>(maps, p, grid, stream, pdl);
       case tc::kModeContigT: return launch_t<128, tc::kModeContigT, 1, false, true>(maps, p, grid, stream, pdl);
+      case tc::kModeA2AC: return launch_t<128, tc::kModeA2AC, 1, false, true>(maps, p, grid, stream, pdl);
       default: return ATTN_A2A_EUNSUPPORTED;
     }
   }
@@ -25,6 +26,7 @@ int launch_fa_tc_split(const tc::Maps<1>& maps, const tc::Params& p, int d, int 
     case tc::kModeA2A: return launch_t<64, tc::kModeA2A, 1, false, true>(maps, p, grid, stream, pdl);
     case tc::kModeA2AT: return launch_t<64, tc::kModeA2AT, 1, false, true>(maps, p, grid, stream, pdl);
     case tc::kModeContigT: return launch_t<64, tc::kModeContigT, 1, false, true>(maps, p, grid, stream, pdl);
+    case tc::kModeA2AC: return launch_t<64, tc::kModeA2AC, 1, false, true>(maps, p, grid, stream, pdl);
     default: return ATTN_A2A_EUNSUPPORTED;
   }
 }

@@ -16,6 +16,7 @@ int launch_fa_tc_traced(const tc::Maps<1>& maps, const tc::Params& p, int d, int
       case tc::kModeA2A: return launch_t<128, tc::kModeA2A, 1, true>(maps, p, grid, stream);
       case tc::kModeA2AT: return launch_t<128, tc::kModeA2AT, 1, true>(maps, p, grid, stream);
       case tc::kModeContigT: return launch_t<128, tc::kModeContigT, 1, true>(maps, p, grid, stream);
+      case tc::kModeA2AC: return launch_t<128, tc::kModeA2AC, 1, true>(maps, p, grid, stream);
       default: return ATTN_A2A_EUNSUPPORTED;
     }
   }
@@ -24,6 +25,7 @@ int launch_fa_tc_traced(const tc::Maps<1>& maps, const tc::Params& p, int d, int
     case tc::kModeA2A: return launch_t<64, tc::kModeA2A, 1, true>(maps, p, grid, stream);
     case tc::kModeA2AT: return launch_t<64, tc::kModeA2AT, 1, true>(maps, p, grid, stream);
     case tc::kModeContigT: return launch_t<64, tc::kModeContigT, 1, true>(maps, p, grid, stream);
+    case tc::kModeA2AC: return launch_t<64, tc::kModeA2AC, 1, true>(maps, p, grid, stream);
     default: return ATTN_A2A_EUNSUPPORTED;
   }
 }

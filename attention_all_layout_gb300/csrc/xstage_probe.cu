@@ -28,6 +28,7 @@ namespace attn_a2a {
 namespace {
 
 constexpr int kProbeThreads = 512;
+constexpr int kRowThreads = 128;  // store_kind 2: the threads that store (one warpgroup)
 constexpr int kBulkChunk = 32768;  // bytes of the shared-memory source of each bulk copy
 // gap_kind 2: operands (two 128 x 64 bf16 swizzle atoms) at a 1024-byte aligned
 // offset after the bulk source, then an mbarrier and the TMEM address slot.
@@ -84,6 +85,19 @@ __global__ void __launch_bounds__(kProbeThreads)
       uint4* b4 = reinterpret_cast<uint4*>(base);
       const long long n = share / 16;
       for (long long i = threadIdx.x; i < n; i += blockDim.x) b4[i] = val;
+    } else if (store_kind == 2) {
+      // whole 256-byte rows, scattered, from one warpgroup: the round's V bytes
+      // are V/256 rows and producer p writes rows p, p + K, p + 2K, ... with
+      // its first 128 threads (16 per row, so a warp's store covers two rows
+      // K * 256 bytes apart), as the fused kernel's tile owner - one
+      // warpgroup - writes its rows with whole-line row stores
+      if (threadIdx.x < kRowThreads) {
+        const uint4 val = make_uint4(static_cast<uint32_t>(r), static_cast<uint32_t>(prod), threadIdx.x, 2u);
+        uint8_t* slot = dst + (r % nslots) * V;
+        const long long nrow = share / 256;
+        for (long long i = threadIdx.x / 16; i < nrow; i += kRowThreads / 16)
+          reinterpret_cast<uint4*>(slot + (i * K + prod) * 256)[threadIdx.x % 16] = val;
+      }
     } else if (threadIdx.x == 0) {
       const uint32_t src = smem_u32(bulk_src);
       for (long long off = 0; off < share; off += kBulkChunk) {
@@ -157,7 +171,7 @@ int launch_probe(const xstage_probe_cfg& c, cudaStream_t stream) {
 int check_probe_cfg(const xstage_probe_cfg& c) {
   if (c.K < 1 || c.K > 1024 || c.rounds < 1) return ATTN_A2A_EINVAL;
   if (c.V_bytes <= 0 || c.V_bytes % (4096ll * c.K) != 0) return ATTN_A2A_EINVAL;
-  if (c.G_ns < 0 || c.store_kind < 0 || c.store_kind > 1 || c.gap_kind < 0 || c.gap_kind > 2)
+  if (c.G_ns < 0 || c.store_kind < 0 || c.store_kind > 2 || c.gap_kind < 0 || c.gap_kind > 2)
     return ATTN_A2A_EINVAL;
   if (c.gap_kind >= 1 && (c.fma_iters < 0 || c.fma_iters > kProbeMaxGapIters)) return ATTN_A2A_EINVAL;
   if (c.stamps == nullptr || (reinterpret_cast<uintptr_t>(c.stamps) & 7u) != 0) return ATTN_A2A_EINVAL;

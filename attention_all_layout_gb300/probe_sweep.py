@@ -37,8 +37,14 @@ def round_volume(v_bytes: float, K: int) -> int:
 
 
 class Prober:
-    def __init__(self, dst_bytes: int, max_stamps: int):
-        self.dst = torch.empty(dst_bytes, dtype=torch.uint8, device="cuda")
+    """Probe launches into one destination buffer: device memory, or with
+    host=True pinned host memory that the GPU stores to over the host link."""
+
+    def __init__(self, dst_bytes: int, max_stamps: int, host: bool = False):
+        if host:
+            self.dst = torch.empty(dst_bytes, dtype=torch.uint8, pin_memory=True)
+        else:
+            self.dst = torch.empty(dst_bytes, dtype=torch.uint8, device="cuda")
         self.stamps = torch.zeros(max_stamps, dtype=torch.int64, device="cuda")
 
     def run(self, K, V, G_ns, rounds, store_kind=0, gap_kind=0, fma_iters=0, discard=None) -> bg.Point:

@@ -447,6 +447,33 @@ def main():
     f1.record(stream)
     barrier()
     ms_e2e = f0.elapsed_time(f1) / e2e_steps
+    # ---- the output partitions in host memory: the tile owners store every row
+    # straight into the host's partitions over the host link (whole-line row
+    # stores), against attention alone, the permute and a copy of the device
+    # partitions to the host (context: the remote-destination case; not the metric)
+    haddr = [t.data_ptr() if t.numel() else 0 for t in hparts]
+
+    def copy_back():
+        with torch.cuda.stream(stream):
+            for a, b_ in zip(hparts, dparts):
+                a.copy_(b_, non_blocking=True)
+
+    def serial_to_host():
+        contig()
+        bd.attn_a2a_permute(o, cfg.P, dparts, stream=stream)
+        copy_back()
+
+    host_legs = {"fused": lambda: bd.attn_a2a_fwd(q, k, v, cfg.P, cfg.scale, haddr, dev_status=status,
+                                                  stream=stream, store_kind=3),
+                 "serial": serial_to_host}
+    host_turns = {name: [] for name in host_legs}
+    for _ in range(3):
+        for name, fn in host_legs.items():
+            host_turns[name].append(time_events(fn, 3, 1, stream))
+    host_med = {name: statistics.median(v) for name, v in host_turns.items()}
+    host_dest = {"fused_into_host_ms": host_med["fused"], "serial_to_host_ms": host_med["serial"],
+                 "speedup_vs_serial": host_med["serial"] / host_med["fused"], "store_kind": 3,
+                 "serial": "attention alone, permute, copy of the partitions to pinned host memory"}
     del hq, hk, hv, dq, dk, dv, dparts, hparts
 
     # ---- the other presets' fused call (context beside the headline; not the metric)
@@ -530,6 +557,7 @@ def main():
         "gpu_launches": args.steps * (2 if ws is not None and device_split_plan(cfg) == "tail" else 1),
         "cpu_baseline": cpu,
         "other_presets_fused": presets or None,
+        "host_destination": host_dest,
     }
     print(json.dumps(line), flush=True)
     if world > 1:

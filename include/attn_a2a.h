@@ -86,8 +86,21 @@ typedef struct {
                                partitions is stored as in 2. All-to-all layout
                                with P > 8: ATTN_A2A_EUNSUPPORTED;
                            2 = vector st.global of each owned output row straight
-                               from registers.
-                           Results are identical; values > 2 are ATTN_A2A_EINVAL */
+                               from registers;
+                           3 = whole-line row stores, all-to-all layout only (else
+                               ATTN_A2A_EUNSUPPORTED): each warp passes its rows
+                               through its own slice of a shared-memory staging
+                               buffer, so that every store instruction writes
+                               whole rows (512 consecutive bytes) instead of a
+                               16-byte piece of each of 32 rows. For partitions
+                               reached over a slower link than the GPU's own
+                               memory, such as host memory that the device can
+                               address (pinned, or coherent on a system with a
+                               coherent host link) or another GPU's memory mapped
+                               into this one's address space: the one kind that
+                               may store there (1 uses tensor maps, made for the
+                               device's own memory). Never chosen automatically.
+                           Results are identical; values > 3 are ATTN_A2A_EINVAL */
   int grid;             /* persistent CTAs; 0 = one per SM */
   long long timeout_ns; /* limit of every in-kernel wait; 0 = 2 000 000 000 ns */
   int inject_stall;     /* test hook, 0 in normal use. 1 = the softmax role of the first
@@ -305,8 +318,15 @@ typedef struct {
   int rounds;            /* rounds per producer, >= 1 */
   long long V_bytes;     /* aggregate burst volume per round; multiple of 4096*K */
   long long G_ns;        /* gap after each burst, ns, >= 0 */
-  int store_kind;        /* 0: st.global.v4 by all producer threads;
-                            1: cp.async.bulk from shared memory, issued by one thread */
+  int store_kind;        /* 0: st.global.v4 by all producer threads, each producer's
+                               share of the burst contiguous;
+                            1: cp.async.bulk from shared memory, issued by one thread;
+                            2: st.global.v4 of whole 256-byte rows, scattered, by
+                               128 threads (one warpgroup) of each producer: the
+                               burst is V/256 rows and producer p writes rows p,
+                               p + K, p + 2K, ... (the pattern of the fused kernel's
+                               whole-line row stores, store_kind 3 there, issued by
+                               the tile owner's warpgroup) */
   int gap_kind;          /* 0: spin on %globaltimer for G_ns (the issuer stays idle);
                             1: dependent FMA chain on every producer thread sized by the
                                host to last about G_ns (the issuer computes);
@@ -403,12 +423,13 @@ int attn_a2a_num_sms(void);
 /* The store kind (attn_a2a_opts.store_kind) an attn_a2a_fwd(_ex) (layout 1)
  * or attn_a2a_fwd_contig(_ex) (layout 0) call would use for its output
  * tiles: 1 = bulk tensor stores from a staging tile, 2 = row stores from
- * registers. S = sequence length, P = partitions (1 for the contiguous
- * layout), layout = 0 contiguous ("attention alone"), 1 all-to-all;
- * store_kind = the requested kind, 0 for the automatic choice. Writes the
- * kind to *resolved (host int) and returns ATTN_A2A_OK;
- * ATTN_A2A_EUNSUPPORTED where store_kind 1 is not built (all-to-all with
- * P > 8); ATTN_A2A_EINVAL for arguments out of range. Host-only, no launch. */
+ * registers, 3 = whole-line row stores. S = sequence length, P = partitions
+ * (1 for the contiguous layout), layout = 0 contiguous ("attention alone"),
+ * 1 all-to-all; store_kind = the requested kind, 0 for the automatic choice.
+ * Writes the kind to *resolved (host int) and returns ATTN_A2A_OK;
+ * ATTN_A2A_EUNSUPPORTED where the kind is not built (1 for all-to-all with
+ * P > 8, 3 for the contiguous layout); ATTN_A2A_EINVAL for arguments out of
+ * range. Host-only, no launch. */
 int attn_a2a_store_kind(int S, int P, int layout, int store_kind, int* resolved);
 
 #ifdef __cplusplus

@@ -88,7 +88,7 @@ def test_fwd_rejects_bad_arguments(lib, kw, code):
 
 def test_bad_options_rejected(lib):
     assert call_fwd(lib, opts=bd._opts(store_kind=7)) == bd.EINVAL
-    assert call_fwd(lib, opts=bd._opts(store_kind=3)) == bd.EINVAL
+    assert call_fwd(lib, opts=bd._opts(store_kind=4)) == bd.EINVAL
     # the bulk-store epilogue exists for the all-to-all layout with at most 8 partitions
     assert call_fwd(lib, P=16, H=16, opts=bd._opts(store_kind=1)) == bd.EUNSUPPORTED
     assert call_fwd(lib, opts=bd._opts(grid=-1)) == bd.EINVAL
@@ -108,9 +108,12 @@ def test_store_kind_query(lib):
     # an explicit kind is kept where it is built
     assert bd.attn_a2a_store_kind(32768, 8, 1, store_kind=1) == 1
     assert bd.attn_a2a_store_kind(1024, 8, 1, store_kind=2) == 2
+    # whole-line row stores: all-to-all layout only, never automatic
+    assert bd.attn_a2a_store_kind(1024, 16, 1, store_kind=3) == 3
     out = ctypes.c_int(0)
     assert lib.attn_a2a_store_kind(4096, 16, 1, 1, ctypes.byref(out)) == bd.EUNSUPPORTED
-    for args in ((4096, 8, 2, 0), (4096, 0, 1, 0), (4096, 65, 1, 0), (-1, 8, 1, 0), (4096, 8, 1, 3)):
+    assert lib.attn_a2a_store_kind(4096, 1, 0, 3, ctypes.byref(out)) == bd.EUNSUPPORTED
+    for args in ((4096, 8, 2, 0), (4096, 0, 1, 0), (4096, 65, 1, 0), (-1, 8, 1, 0), (4096, 8, 1, 4)):
         assert lib.attn_a2a_store_kind(*args, ctypes.byref(out)) == bd.EINVAL
     assert lib.attn_a2a_store_kind(4096, 8, 1, 0, None) == bd.EINVAL
 
@@ -124,7 +127,10 @@ def test_empty_problem_is_ok_without_launch(lib):
 def test_contig_and_permute_validation(lib):
     shp = bd.plain_shape(1, 4, 256, 64)
     assert lib.attn_a2a_fwd_contig_ex(FAKE, FAKE * 2, FAKE * 3, ctypes.byref(shp), 0.1, FAKE * 16, None,
-                                      ctypes.byref(bd._opts(store_kind=3)), None) == bd.EINVAL
+                                      ctypes.byref(bd._opts(store_kind=4)), None) == bd.EINVAL
+    # whole-line row stores are built for the all-to-all layout only (refused before any launch)
+    assert lib.attn_a2a_fwd_contig_ex(FAKE, FAKE * 2, FAKE * 3, ctypes.byref(shp), 0.1, FAKE * 16, None,
+                                      ctypes.byref(bd._opts(store_kind=3)), None) == bd.EUNSUPPORTED
     assert lib.attn_a2a_fwd_contig(FAKE, FAKE * 2, FAKE * 3, ctypes.byref(shp), 0.1, None, None, None) == bd.EINVAL
     # output overlapping q
     assert lib.attn_a2a_fwd_contig(FAKE, FAKE * 4, FAKE * 8, ctypes.byref(shp), 0.1, FAKE + 64, None, None) == bd.EINVAL
@@ -148,7 +154,7 @@ def test_probe_validation(lib):
     assert run(rounds=0) == bd.EINVAL
     assert run(V_bytes=4096 * 4 + 16) == bd.EINVAL
     assert run(dst_bytes=4096) == bd.EINVAL
-    assert run(store_kind=2) == bd.EINVAL
+    assert run(store_kind=3) == bd.EINVAL
     assert run(G_ns=-1) == bd.EINVAL
     assert run(stamps=0) == bd.EINVAL
     assert run(dst=FAKE + 4) == bd.EINVAL
@@ -181,7 +187,7 @@ def test_noalloc_probe_validation(lib):
 # status for each (they share their field checks; only the burst target differs).
 BAD_PROBE_FIELDS = [
     dict(K=0), dict(K=1025), dict(rounds=0), dict(V_bytes=0), dict(V_bytes=4096 * 4 + 16),
-    dict(G_ns=-1), dict(store_kind=-1), dict(store_kind=2), dict(gap_kind=-1), dict(gap_kind=3),
+    dict(G_ns=-1), dict(store_kind=-1), dict(store_kind=3), dict(gap_kind=-1), dict(gap_kind=3),
     dict(gap_kind=1, fma_iters=-1), dict(gap_kind=1, fma_iters=10**8 + 1),
     dict(gap_kind=2, fma_iters=-1), dict(gap_kind=2, fma_iters=10**8 + 1),
     dict(stamps=0), dict(stamps=FAKE + 4),

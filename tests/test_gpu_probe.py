@@ -21,7 +21,7 @@ def prober():
     return ps.Prober(dst_bytes, K * 64 * 3), K
 
 
-@pytest.mark.parametrize("kind", [0, 1])
+@pytest.mark.parametrize("kind", [0, 1, 2])
 def test_stamps_are_ordered_and_gaps_honoured(prober, kind):
     pr, K = prober
     V = ps.round_volume(8 * 2**20, K)
@@ -82,3 +82,31 @@ def test_mma_gap_kind(prober, kind):
     torch.cuda.synchronize()
     s = st.view(K, 8, 3).cpu()
     assert torch.all(s[:, :, 1] >= s[:, :, 0]) and torch.all(s[:, :, 2] >= s[:, :, 1])
+
+
+@pytest.fixture(scope="module")
+def host_prober():
+    K = bd.num_sms()
+    dst_bytes = (4 * 64 * 2**20 // (4096 * K) + 1) * 4096 * K
+    return ps.Prober(dst_bytes, K * 16 * 3, host=True), K
+
+
+@pytest.mark.parametrize("kind", [0, 2])
+def test_host_destination_fit(host_prober, kind):
+    """Bursts into pinned host memory, drained over the host link: a large
+    burst with no gap is drain-dominated, a long gap brings the issue time to
+    its floor, and the equation fitted on part of the sweep predicts the
+    held-out points within 15 %."""
+    pr, K = host_prober
+    pts = []
+    for vmb in (4, 16, 64):
+        for g in (0, 10, 40, 100, 400):
+            pts.append(pr.run(K, ps.round_volume(vmb * 2**20, K), g * 1000, 16, store_kind=kind, discard=8))
+    V64 = ps.round_volume(64 * 2**20, K)
+    p0 = next(p for p in pts if p.V == V64 and p.G == 0)
+    p400 = next(p for p in pts if p.V == V64 and p.G == 400e-6)
+    assert p0.t_iss_med > 5 * p400.t_iss_med
+    f, held = ps.split_fit(pts, seed=2, g_max=400e-6)
+    print(f"host destination, kind {kind}: R = {f.R / 1e9:.0f} GB/s, Q = {f.Q}, held-out {held}")
+    assert held["n"] >= 3
+    assert held["median_abs_rel"] <= 0.15

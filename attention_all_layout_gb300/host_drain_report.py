@@ -17,7 +17,11 @@ next tiles compute.
    lines (probe store_kind 0) and scattered whole rows (store_kind 2, the
    epilogue's pattern), idle gaps, each with held-out residuals.
 2. Per workload, legs taking turns over several rounds (median per leg):
-   fused into host partitions (fh), the same into device partitions (fd),
+   fused into host partitions (fh), the same with a workspace so that the
+   library's automatic split schedule applies (fhs: where it splits, CTAs
+   finish their tiles at staggered times instead of in waves), the same with
+   every item's key blocks split into equal ranges whatever the automatic
+   choice (fha), the same into device partitions (fd),
    attention alone into device memory (c), the separate permute (p), and the
    copy of the device partitions to the host (x, one contiguous copy per
    partition). Serial baseline = c + p + x; fused then copy = fd + x. The
@@ -122,8 +126,12 @@ def measure(cfg, R: float, n_sm: int, trace: bool = True) -> dict:
         for a, b in zip(hparts, dparts):
             a.copy_(b, non_blocking=True)
 
+    ws = bd.alloc_workspace(cfg.d)
     legs = {
         "fh": lambda: bd.attn_a2a_fwd(q, k, v, cfg.P, cfg.scale, haddr, store_kind=3),
+        "fhs": lambda: bd.attn_a2a_fwd(q, k, v, cfg.P, cfg.scale, haddr, store_kind=3, workspace=ws),
+        "fha": lambda: bd.attn_a2a_fwd(q, k, v, cfg.P, cfg.scale, haddr, store_kind=3, workspace=ws,
+                                       split=bd.SPLIT_ALL),
         "fd": lambda: bd.attn_a2a_fwd(q, k, v, cfg.P, cfg.scale, dparts, store_kind=3),
         "c": lambda: bd.attn_a2a_fwd_contig(q, k, v, cfg.scale, o),
         "p": lambda: bd.attn_a2a_permute(o, cfg.P, dparts),
@@ -140,7 +148,8 @@ def measure(cfg, R: float, n_sm: int, trace: bool = True) -> dict:
     serial = med["c"] + med["p"] + med["x"]
     row = {"workload": cfg.name, "B": cfg.B, "H": cfg.H, "S": cfg.S, "d": cfg.d, "P": cfg.P,
            "bytes_equal": same, "out_MB": out_bytes / 2**20,
-           "fused_host_ms": med["fh"], "fused_device_ms": med["fd"], "attention_alone_ms": med["c"],
+           "fused_host_ms": med["fh"], "fused_host_split_ms": med["fhs"], "fused_host_split_all_ms": med["fha"],
+           "split": split_kind(cfg, n_sm), "fused_device_ms": med["fd"], "attention_alone_ms": med["c"],
            "permute_ms": med["p"], "copy_to_host_ms": med["x"], "serial_ms": serial,
            "fused_then_copy_ms": med["fd"] + med["x"], "speedup_vs_serial": serial / med["fh"],
            "speedup_vs_fused_then_copy": (med["fd"] + med["x"]) / med["fh"],
@@ -160,9 +169,27 @@ def measure(cfg, R: float, n_sm: int, trace: bool = True) -> dict:
         torch.cuda.synchronize()
         row["traced_device"] = tt.summary(tt.records(tr, cfg.B, cfg.H, cfg.S), cfg.S, min(n_sm, items))
         del tr
-    del q, k, v, dparts, hparts, o
+    del q, k, v, dparts, hparts, o, ws
     torch.cuda.empty_cache()
     return row
+
+
+def split_kind(cfg, n_sm: int):
+    """The split the library picks automatically for cfg with a workspace (its
+    rule restated): "all", "tail" or None."""
+    nblk = (cfg.S + 127) // 128
+    total = cfg.B * cfg.H * ((nblk + 1) // 2)
+    grid = min(n_sm, total)
+    if nblk < 2:
+        return None
+    waves = (total + grid - 1) // grid
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    if 2 * 4 * cfg.B * cfg.H * cfg.S * cfg.d <= l2 and waves * nblk - (total * nblk + grid - 1) // grid >= 4:
+        return "all"
+    r = total - (waves - 1) * grid
+    if r < grid and nblk - (r * nblk + grid - 1) // grid >= 32:
+        return "tail"
+    return None
 
 
 def report(H=40, d=128, P=8, s_list=S_LIST, presets=PRESETS, quick=False) -> dict:
@@ -204,6 +231,9 @@ def main(argv=None) -> int:
               f"{ma['burst_gap_ms']:.3f} ({100 * ma['burst_gap_rel_err']:+.0f} %); coupled "
               f"{ma['completion_coupled_ms']:.3f}, async {ma['unbounded_async_ms']:.3f}; bytes equal {r['bytes_equal']}")
     print(f"R from the fused call at {res['R_app_from']}: {res['R_app_GBps']:.1f} GB/s")
+    for r in res["rows"]:
+        print(f"{r['workload']:>7}: fused->host with the automatic split ({r['split']}) {r['fused_host_split_ms']:.3f} ms, "
+              f"whole schedule split {r['fused_host_split_all_ms']:.3f} ms, without {r['fused_host_ms']:.3f} ms")
     for k, f in res["fits"].items():
         print(f"fit {k}: R {f['R_GBps']:.1f} GB/s, Q {f['Q_MB']} MB, held-out {f['heldout']}")
     return 0

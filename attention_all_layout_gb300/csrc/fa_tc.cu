@@ -17,26 +17,38 @@ namespace attn_a2a {
 namespace {
 
 // Longest sequence, in 128-row key blocks, for which the automatic store kind
-// picks bulk tensor stores for the all-to-all layout (S <= 16384). Measured
-// at H = 40, d = 128, P = 8 (bulk / row stores): S = 8192 0.978, 12288
-// 0.997, 16384 0.999, 24576 1.008, 32768 1.004, 75600 1.008.
-constexpr int kBulkA2AMaxBlocks = 128;
+// picks bulk tensor stores for the all-to-all layout (S <= 32768). Measured
+// at H = 40, d = 128, P = 8 on the current kernel (bulk / row stores, calls
+// alternating, median of pairs): S = 24576 0.988, 32768 0.993 (bench-length
+// turns: 13.70 against 13.79 ms), 75600 1.003. (The first kernel measured
+// 1.008 at 24576 and 1.004 at 32768, when the boundary was S = 16384.)
+constexpr int kBulkA2AMaxBlocks = 256;
+// The same boundary for the whole Ulysses layer (sequence-sharded inputs):
+// there bulk stores also mean tiles counted over the whole sequence
+// (kModeS2SGT), measured against the per-partition tiles of kModeS2S only up
+// to S = 16384.
+constexpr int kBulkS2SMaxBlocks = 128;
 
 }  // namespace
 
 // store_kind 0: bulk tensor stores where they are built and measured faster -
 // the contiguous layout, and the all-to-all layout with up to kMaxStoreMaps
-// partitions and at most kBulkA2AMaxBlocks key blocks (at longer sequences its
-// strided tile stores measured slower than row stores) - else row stores;
+// partitions and at most max_bulk_blocks key blocks (at longer sequences its
+// strided tile stores measured level with or slower than row stores) - else
+// row stores;
 // 1: bulk stores, or 0 where they are not built; 2: row stores; 3: row stores
 // written as whole lines through shared memory (all-to-all layout only, else 0).
-int resolve_store_kind(int S, int P, bool a2a, int store_kind) {
+int resolve_store_kind(int S, int P, bool a2a, int store_kind, int max_bulk_blocks) {
   const bool built = !a2a || P <= tc::kMaxStoreMaps;
   if (store_kind == 1) return built ? 1 : 0;
   if (store_kind == 2) return 2;
   if (store_kind == 3) return a2a ? 3 : 0;
-  const bool faster = !a2a || (S + tc::kBM - 1) / tc::kBM <= kBulkA2AMaxBlocks;
+  const bool faster = !a2a || (S + tc::kBM - 1) / tc::kBM <= max_bulk_blocks;
   return built && faster ? 1 : 2;
+}
+
+int resolve_store_kind(int S, int P, bool a2a, int store_kind) {
+  return resolve_store_kind(S, P, a2a, store_kind, kBulkA2AMaxBlocks);
 }
 
 namespace {
@@ -292,7 +304,7 @@ int launch_fa_tc_s2s(const void* const* qp, const void* const* kp, const void* c
   // measured 1.4 % faster than with row stores), else the per-partition tiles
   // of kModeS2S (measured 1-2 % faster than kModeS2SG at S = 32768). Other
   // partition lengths count tiles per partition (kModeS2S).
-  const int auto_kind = resolve_store_kind(shp.S, epi.P, true, opts.store_kind);
+  const int auto_kind = resolve_store_kind(shp.S, epi.P, true, opts.store_kind, kBulkS2SMaxBlocks);
   if (auto_kind == 0) return ATTN_A2A_EUNSUPPORTED;
   const bool equal64 = epi.crem == 0 && epi.cbase > 0 && epi.cbase % (tc::kBM / 2) == 0;
   const int seg = epi.cbase % tc::kBM == 0 ? tc::kBM : tc::kBM / 2;

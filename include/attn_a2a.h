@@ -77,7 +77,7 @@ typedef struct {
 typedef struct {
   int store_kind;       /* how the tile owner stores its output tile:
                            0 = automatic: 1 for the contiguous layout and for the
-                               all-to-all layout with P <= 8 and S <= 16384 (where
+                               all-to-all layout with P <= 8 and S <= 32768 (where
                                it measured faster), else 2;
                            1 = bulk tensor stores (TMA) from a shared-memory staging
                                tile: the owner commits the bulk group and resumes,

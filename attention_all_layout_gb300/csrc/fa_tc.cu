@@ -207,6 +207,32 @@ int grid_for(const tc::Params& p, const attn_a2a_opts& opts) {
   return grid > p.total ? p.total : grid;
 }
 
+// 1 when every output buffer that receives rows (the partitions with rows, or
+// the contiguous output) is memory of the current device, 0 when one is not
+// (host memory, including pinned or coherent host memory the device can
+// store to, managed memory, another device's memory), -1 on a CUDA error.
+int outputs_in_device_memory(bool a2a, const EpiParams& epi, const attn_a2a_shape& shp) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  auto on_device = [dev](const void* ptr) -> int {
+    cudaPointerAttributes attr;
+    if (cudaPointerGetAttributes(&attr, ptr) != cudaSuccess) {
+      cudaGetLastError();
+      return -1;
+    }
+    return attr.type == cudaMemoryTypeDevice && attr.device == dev ? 1 : 0;
+  };
+  if (!a2a) return on_device(epi.out);
+  for (int j = 0; j < epi.P; ++j) {
+    const int c = epi.cbase + (j < epi.crem ? 1 : 0);
+    if (c == 0) continue;
+    const int r = on_device(epi.part[j]);
+    if (r != 1) return r;
+  }
+  (void)shp;
+  return 1;
+}
+
 }  // namespace
 
 int launch_plain(const tc::Maps<1>& maps, const tc::Params& p, int d, int mode, int grid, cudaStream_t stream);
@@ -216,8 +242,20 @@ int launch_fa_tc(const void* q, const void* k, const void* v, const attn_a2a_sha
                  const attn_a2a_opts& opts, cudaStream_t stream) {
   tc::Maps<1> maps;
   std::memset(&maps, 0, sizeof(maps));
-  const int kind = resolve_store_kind(shp.S, epi.P, a2a, opts.store_kind);
+  int kind = resolve_store_kind(shp.S, epi.P, a2a, opts.store_kind);
   if (kind == 0) return ATTN_A2A_EUNSUPPORTED;
+  if (kind == 1) {
+    // bulk tensor stores go through tensor maps made for this device's memory:
+    // outputs elsewhere (host memory the device can address, for one) take
+    // the whole-line row stores (all-to-all) or the row stores (contiguous)
+    // when the kind is automatic, and are refused when bulk stores were asked for
+    const int dev_rc = outputs_in_device_memory(a2a, epi, shp);
+    if (dev_rc < 0) return ATTN_A2A_ECUDA;
+    if (dev_rc == 0) {
+      if (opts.store_kind == 1) return ATTN_A2A_EUNSUPPORTED;
+      kind = a2a ? 3 : 2;
+    }
+  }
   const bool bulk = kind == 1;
   if (bulk && a2a) {
     const int h_row = epi.hstride > 0 ? epi.hstride : shp.H;
@@ -304,8 +342,16 @@ int launch_fa_tc_s2s(const void* const* qp, const void* const* kp, const void* c
   // measured 1.4 % faster than with row stores), else the per-partition tiles
   // of kModeS2S (measured 1-2 % faster than kModeS2SG at S = 32768). Other
   // partition lengths count tiles per partition (kModeS2S).
-  const int auto_kind = resolve_store_kind(shp.S, epi.P, true, opts.store_kind, kBulkS2SMaxBlocks);
+  int auto_kind = resolve_store_kind(shp.S, epi.P, true, opts.store_kind, kBulkS2SMaxBlocks);
   if (auto_kind == 0) return ATTN_A2A_EUNSUPPORTED;
+  if (auto_kind == 1) {  // bulk stores only into this device's memory (see launch_fa_tc)
+    const int dev_rc = outputs_in_device_memory(true, epi, shp);
+    if (dev_rc < 0) return ATTN_A2A_ECUDA;
+    if (dev_rc == 0) {
+      if (opts.store_kind == 1) return ATTN_A2A_EUNSUPPORTED;
+      auto_kind = 2;
+    }
+  }
   const bool equal64 = epi.crem == 0 && epi.cbase > 0 && epi.cbase % (tc::kBM / 2) == 0;
   const int seg = epi.cbase % tc::kBM == 0 ? tc::kBM : tc::kBM / 2;
   const bool global_tiles = equal64 && (seg < tc::kBM || auto_kind == 1);

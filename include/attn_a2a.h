@@ -78,13 +78,19 @@ typedef struct {
   int store_kind;       /* how the tile owner stores its output tile:
                            0 = automatic: 1 for the contiguous layout and for the
                                all-to-all layout with P <= 8 and S <= 32768 (where
-                               it measured faster), else 2;
+                               it measured faster), else 2; where 1 would be chosen
+                               but an output buffer is not memory of the current
+                               device (cudaPointerGetAttributes: host memory the
+                               device can address, managed memory, another
+                               device's memory), 3 for the all-to-all layout and 2
+                               for the contiguous one;
                            1 = bulk tensor stores (TMA) from a shared-memory staging
                                tile: the owner commits the bulk group and resumes,
                                waiting only until the stores have read the staging
                                tile before reusing it; a tile that straddles two
                                partitions is stored as in 2. All-to-all layout
-                               with P > 8: ATTN_A2A_EUNSUPPORTED;
+                               with P > 8, or an output buffer that is not memory
+                               of the current device: ATTN_A2A_EUNSUPPORTED;
                            2 = vector st.global of each owned output row straight
                                from registers;
                            3 = whole-line row stores, all-to-all layout only (else
@@ -97,9 +103,12 @@ typedef struct {
                                memory, such as host memory that the device can
                                address (pinned, or coherent on a system with a
                                coherent host link) or another GPU's memory mapped
-                               into this one's address space: the one kind that
-                               may store there (1 uses tensor maps, made for the
-                               device's own memory). Never chosen automatically.
+                               into this one's address space (1 uses tensor maps,
+                               made for the device's own memory, and is refused
+                               there; 2 stores 16-byte pieces of 32 rows at a time,
+                               which such links drain far more slowly). Chosen
+                               automatically only in place of 1 for outputs outside
+                               the device's memory.
                            Results are identical; values > 3 are ATTN_A2A_EINVAL */
   int grid;             /* persistent CTAs; 0 = one per SM */
   long long timeout_ns; /* limit of every in-kernel wait; 0 = 2 000 000 000 ns */

@@ -87,8 +87,10 @@ def test_line_stores_traced():
 
 
 @pytest.mark.parametrize("name", ["small", "image"])
-@pytest.mark.parametrize("store_kind", [2, 3])
+@pytest.mark.parametrize("store_kind", [0, 2, 3])
 def test_partitions_in_host_memory(name, store_kind):
+    # kind 0 (automatic) would take bulk stores for device partitions at these
+    # sizes; for host partitions the library takes the whole-line row stores
     cfg = (workloads.AttnConfig("host", B=1, H=3, S=1000, d=128, P=3) if name == "small"
            else workloads.CONFIGS["image"])
     q, k, v = workloads.make_qkv(cfg, seed=9, device="cuda")
@@ -101,3 +103,20 @@ def test_partitions_in_host_memory(name, store_kind):
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     assert same_bytes(host, [t.cpu() for t in dev])
+
+
+def test_bulk_stores_refused_outside_device_memory():
+    cfg = workloads.AttnConfig("host", B=1, H=2, S=512, d=128, P=2)
+    q, k, v = workloads.make_qkv(cfg, seed=10, device="cuda")
+    host = [torch.zeros(t, dtype=torch.bfloat16, pin_memory=True) for t in
+            [(1, c, cfg.H, cfg.d) for c in bd.chunk_sizes(cfg.S, cfg.P)]]
+    assert bd.attn_a2a_fwd(q, k, v, cfg.P, cfg.scale, [t.data_ptr() for t in host], store_kind=1,
+                           check=False) == bd.EUNSUPPORTED
+    o = torch.zeros((1, cfg.H, cfg.S, cfg.d), dtype=torch.bfloat16, pin_memory=True)
+    assert bd.attn_a2a_fwd_contig(q, k, v, cfg.scale, o, store_kind=1, check=False) == bd.EUNSUPPORTED
+    # the automatic kind stores the contiguous output into host memory with row stores
+    dev = torch.empty((1, cfg.H, cfg.S, cfg.d), dtype=torch.bfloat16, device="cuda")
+    bd.attn_a2a_fwd_contig(q, k, v, cfg.scale, dev)
+    bd.attn_a2a_fwd_contig(q, k, v, cfg.scale, o)
+    torch.cuda.synchronize()
+    assert torch.equal(o.view(torch.int16), dev.cpu().view(torch.int16))

@@ -24,8 +24,11 @@ next tiles compute.
    choice (fha), the same into device partitions (fd),
    attention alone into device memory (c), the separate permute (p), and the
    copy of the device partitions to the host (x, one contiguous copy per
-   partition). Serial baseline = c + p + x; fused then copy = fd + x. The
-   host partitions are checked byte for byte against the device ones.
+   partition). Serial baseline = c + p + x; fused then copy = fd + x. And one
+   Ulysses rank's view: its own partition in device memory, the other P - 1 in
+   host memory, automatic store kind (fr), against c + p + the copy of the
+   P - 1 partitions (xr). The host partitions are checked byte for byte
+   against the device ones.
 3. The equation's prediction of fh, per wave of work items (all CTAs finish
    an item together; the last wave may be partial): the wave's stores,
    V_w = items_w * 2 * 128 * 2d bytes, cost the issuers max(0, V_w/R - G)
@@ -121,9 +124,25 @@ def measure(cfg, R: float, n_sm: int, trace: bool = True) -> dict:
     bd.attn_a2a_fwd(q, k, v, cfg.P, cfg.scale, haddr, store_kind=3)
     torch.cuda.synchronize()
     same = all(torch.equal(a.view(torch.int16), b.cpu().view(torch.int16)) for a, b in zip(hparts, dparts))
+    own = dparts[0].clone()
+    for t in hparts:
+        t.zero_()
+    dparts[0].zero_()
+    bd.attn_a2a_fwd(q, k, v, cfg.P, cfg.scale, [dparts[0].data_ptr()] + haddr[1:])
+    torch.cuda.synchronize()
+    same = same and torch.equal(own.view(torch.int16), dparts[0].view(torch.int16)) and all(
+        torch.equal(a.view(torch.int16), b.cpu().view(torch.int16)) for a, b in zip(hparts[1:], dparts[1:]))
 
     def copy_back():
         for a, b in zip(hparts, dparts):
+            a.copy_(b, non_blocking=True)
+
+    # one Ulysses rank's view: its own partition in device memory, the other
+    # P - 1 (the other ranks') in host memory; the automatic store kind
+    raddr = [dparts[0].data_ptr()] + haddr[1:]
+
+    def copy_back_remote():
+        for a, b in zip(hparts[1:], dparts[1:]):
             a.copy_(b, non_blocking=True)
 
     ws = bd.alloc_workspace(cfg.d)
@@ -136,6 +155,8 @@ def measure(cfg, R: float, n_sm: int, trace: bool = True) -> dict:
         "c": lambda: bd.attn_a2a_fwd_contig(q, k, v, cfg.scale, o),
         "p": lambda: bd.attn_a2a_permute(o, cfg.P, dparts),
         "x": copy_back,
+        "fr": lambda: bd.attn_a2a_fwd(q, k, v, cfg.P, cfg.scale, raddr),
+        "xr": copy_back_remote,
     }
     n = max(3, min(50, int(5e11 / cfg.flops))) if cfg.flops < 5e12 else 3
     samples = {name: [] for name in legs}
@@ -154,7 +175,9 @@ def measure(cfg, R: float, n_sm: int, trace: bool = True) -> dict:
            "fused_then_copy_ms": med["fd"] + med["x"], "speedup_vs_serial": serial / med["fh"],
            "speedup_vs_fused_then_copy": (med["fd"] + med["x"]) / med["fh"],
            "host_over_device": med["fh"] / med["fd"] - 1,
-           "effective_drain_GBps": out_bytes / (med["fh"] * 1e-3) / 1e9}
+           "effective_drain_GBps": out_bytes / (med["fh"] * 1e-3) / 1e9,
+           "rank_fused_ms": med["fr"], "rank_serial_ms": med["c"] + med["p"] + med["xr"],
+           "rank_speedup_vs_serial": (med["c"] + med["p"] + med["xr"]) / med["fr"]}
     row["model"] = predict(med["fd"], med["c"], items, min(n_sm, items), 2 * 128 * 2 * cfg.d, out_bytes, R)
     row["model"]["burst_gap_rel_err"] = row["model"]["burst_gap_ms"] / med["fh"] - 1
     if trace:
@@ -231,6 +254,9 @@ def main(argv=None) -> int:
               f"{ma['burst_gap_ms']:.3f} ({100 * ma['burst_gap_rel_err']:+.0f} %); coupled "
               f"{ma['completion_coupled_ms']:.3f}, async {ma['unbounded_async_ms']:.3f}; bytes equal {r['bytes_equal']}")
     print(f"R from the fused call at {res['R_app_from']}: {res['R_app_GBps']:.1f} GB/s")
+    for r in res["rows"]:
+        print(f"{r['workload']:>7}: one rank's view (own partition local, P - 1 in host memory): fused "
+              f"{r['rank_fused_ms']:.3f} ms, serial {r['rank_serial_ms']:.3f} ({r['rank_speedup_vs_serial']:.2f}x)")
     for r in res["rows"]:
         print(f"{r['workload']:>7}: fused->host with the automatic split ({r['split']}) {r['fused_host_split_ms']:.3f} ms, "
               f"whole schedule split {r['fused_host_split_all_ms']:.3f} ms, without {r['fused_host_ms']:.3f} ms")

@@ -388,6 +388,21 @@ int attn_a2a_fwd_host(const void* hq, const void* hk, const void* hv, const attn
                         tensor_span(dv, s.B, s.H, s.S, s.d, s.v_sb, s.v_sh, s.v_ss)};
     if (partitions_alias_inputs(s, epi, in, 3)) return ATTN_A2A_EINVAL;
   }
+  // Host partitions that are pinned host memory (which the device can store
+  // to) receive the rows straight from the kernels, as whole-line row stores
+  // over the host link, and no copy back is needed; otherwise the kernels
+  // store into dparts and each chunk is copied back.
+  bool direct = true;
+  for (int j = 0; j < P && direct; ++j) {
+    if (epi.cbase + (j < epi.crem ? 1 : 0) == 0) continue;
+    cudaPointerAttributes attr;
+    if (cudaPointerGetAttributes(&attr, hparts[j]) != cudaSuccess) {
+      cudaGetLastError();
+      direct = false;
+    } else {
+      direct = attr.type == cudaMemoryTypeHost;
+    }
+  }
   HostPipe* hp = host_pipe();
   if (hp == nullptr) return ATTN_A2A_ECUDA;
   std::lock_guard<std::mutex> lock(hp->mu);
@@ -404,7 +419,9 @@ int attn_a2a_fwd_host(const void* hq, const void* hk, const void* hv, const attn
   if (cudaEventRecord(hp->ev_start, st) != cudaSuccess || cudaStreamWaitEvent(hp->h2d, hp->ev_start, 0) != cudaSuccess ||
       cudaStreamWaitEvent(hp->comp2, hp->ev_start, 0) != cudaSuccess)
     return ATTN_A2A_ECUDA;
-  const attn_a2a_opts o = default_opts();
+  attn_a2a_opts o = default_opts();
+  if (direct) o.store_kind = 3;
+  void* const* outs = direct ? hparts : dparts;
   int launch = 0;
   for (int b = 0; b < s.B; ++b) {
     for (int ci = 0, h0 = 0; ci < nchunk; h0 += chunk[ci], ++ci, ++launch) {
@@ -428,7 +445,7 @@ int attn_a2a_fwd_host(const void* hq, const void* hk, const void* hv, const attn
       ce.hstride = s.H;
       for (int j = 0; j < P; ++j) {
         const int c = epi.cbase + (j < epi.crem ? 1 : 0);
-        ce.part[j] = c > 0 ? static_cast<void*>(static_cast<uint16_t*>(dparts[j]) +
+        ce.part[j] = c > 0 ? static_cast<void*>(static_cast<uint16_t*>(outs[j]) +
                                                  (static_cast<size_t>(b) * c * s.H + h0) * s.d)
                            : nullptr;
       }
@@ -438,7 +455,7 @@ int attn_a2a_fwd_host(const void* hq, const void* hk, const void* hv, const attn
       if (cudaEventRecord(hp->ev_comp, cs_stream) != cudaSuccess ||
           cudaStreamWaitEvent(hp->d2h, hp->ev_comp, 0) != cudaSuccess)
         return ATTN_A2A_ECUDA;
-      for (int j = 0; j < P; ++j) {
+      for (int j = 0; j < P && !direct; ++j) {
         const int c = epi.cbase + (j < epi.crem ? 1 : 0);
         if (c == 0) continue;
         const size_t eoff = (static_cast<size_t>(b) * c * s.H + h0) * s.d;
@@ -452,7 +469,8 @@ int attn_a2a_fwd_host(const void* hq, const void* hk, const void* hv, const attn
     }
   }
   // the caller's stream completes only when the last copy back has (which
-  // follows every chunk's kernel, on either stream)
+  // follows every chunk's kernel, on either stream; with direct stores the
+  // copy stream only waits for the kernels)
   if (cudaEventRecord(hp->ev_end, hp->d2h) != cudaSuccess || cudaStreamWaitEvent(st, hp->ev_end, 0) != cudaSuccess)
     return ATTN_A2A_ECUDA;
   return ATTN_A2A_OK;

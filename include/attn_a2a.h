@@ -292,8 +292,13 @@ int attn_a2a_fwd_simt(const void* q, const void* k, const void* v, const attn_a2
  * attn_a2a_fwd_host - the product call from host memory, for callers whose
  * data lives on the host: copies q, k, v (host, contiguous [B,H,S,d] bf16,
  * pinned for asynchronous copies) into the caller's device buffers dq, dk,
- * dv, runs the fused attention into the caller's device partitions dparts[j],
- * and copies each partition back into hparts[j] (host). The heads are
+ * dv, runs the fused attention and delivers the partitions into hparts[j]
+ * (host): when every hparts[j] with rows is pinned host memory
+ * (cudaPointerGetAttributes type cudaMemoryTypeHost), the kernels store each
+ * output row straight into it over the host link (whole-line row stores,
+ * store_kind 3) and dparts is not written; otherwise they store into the
+ * caller's device partitions dparts[j], copied back into hparts[j]. hparts
+ * must not overlap hq, hk or hv. The heads are
  * processed in up to eight chunks - small first and last ones, so that
  * little copying is exposed before the first kernel and after the last - so
  * that the copies of one chunk overlap the kernel of another; the copies run

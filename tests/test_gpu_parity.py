@@ -142,21 +142,26 @@ def test_empty_sequence_launches_nothing():
     assert bd.attn_a2a_fwd(q, q, q, 2, 0.1, [None, None]) == bd.OK
 
 
+@pytest.mark.parametrize("pinned", [True, False])
 @pytest.mark.parametrize("B,H,S", [(1, 4, 1500), (2, 16, 640), (1, 40, 300)])
-def test_host_entry_point_matches_device_path(B, H, S):
+def test_host_entry_point_matches_device_path(B, H, S, pinned):
     # head chunks: one head each for H = 4; a ramp (1, 3, 8, 3, 1 heads) per
-    # batch entry for H = 16; the video head count (1, 3, 8, 20, 7, 1) for H = 40
+    # batch entry for H = 16; the video head count (1, 3, 8, 20, 7, 1) for H = 40.
+    # Pinned host partitions receive the rows straight from the kernels (the
+    # device partitions stay untouched); pageable ones by copies from dparts
     cfg = workloads.config("image", B=B, H=H, S=S)
     q, k, v = workloads.make_qkv(cfg, seed=5)
     hq, hk, hv = (t.pin_memory() for t in (q, k, v))
     dq, dk, dv = (torch.empty_like(t, device="cuda") for t in (q, k, v))
-    dparts = bd.alloc_partitions(cfg.B, cfg.S, cfg.H, cfg.d, cfg.P)
-    hparts = [torch.empty_like(p, device="cpu").pin_memory() for p in dparts]
+    dparts = bd.alloc_partitions(cfg.B, cfg.S, cfg.H, cfg.d, cfg.P, fill=7.0)
+    hparts = [torch.zeros(p.shape, dtype=p.dtype, pin_memory=pinned) for p in dparts]
     bd.attn_a2a_fwd_host(hq, hk, hv, cfg.P, cfg.scale, dq, dk, dv, dparts, hparts)
     torch.cuda.synchronize()
     ref = fused(q.cuda(), k.cuda(), v.cuda(), cfg.P, cfg.scale)
     for a, b in zip(hparts, ref.parts):
         assert torch.equal(a.view(torch.int16), b.cpu().view(torch.int16))
+    for d in dparts:
+        assert bool(torch.all(d == 7.0)) == pinned
 
 
 def test_bounded_wait_reports_timeout_and_context_survives():

@@ -8,8 +8,10 @@ resident in HBM (1.0 GB of q, k, v: larger than L2, so no flush is needed).
 
 Prints one JSON line. Legs:
   value        device-timed fused call, TFLOP/s = 4*B*H*S^2*d / time
-  e2e          the host-memory C-ABI call (pinned host q, k, v -> device,
-               fused kernel, partitions -> pinned host) timed end to end
+  e2e          the host-memory C-ABI call (pinned host q, k, v copied to the
+               device, fused kernels whose tile owners store the output rows
+               straight into the pinned host partitions) timed end to end;
+               d2h_bytes_per_step counts the output those stores carry
   roofline     the fused kernel against the measured bf16 tensor peak
   cpu_baseline the float64 oracle on a bounded row sample, on host cores
   attention-alone, serial (attention, then a separate permute) and whole-layer

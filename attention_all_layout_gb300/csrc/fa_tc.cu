@@ -244,11 +244,13 @@ int launch_fa_tc(const void* q, const void* k, const void* v, const attn_a2a_sha
   std::memset(&maps, 0, sizeof(maps));
   int kind = resolve_store_kind(shp.S, epi.P, a2a, opts.store_kind);
   if (kind == 0) return ATTN_A2A_EUNSUPPORTED;
-  if (kind == 1) {
-    // bulk tensor stores go through tensor maps made for this device's memory:
-    // outputs elsewhere (host memory the device can address, for one) take
-    // the whole-line row stores (all-to-all) or the row stores (contiguous)
-    // when the kind is automatic, and are refused when bulk stores were asked for
+  if (kind == 1 || (opts.store_kind == 0 && a2a)) {
+    // Bulk tensor stores go through tensor maps made for this device's memory:
+    // outputs elsewhere (host memory the device can address, for one) take the
+    // whole-line row stores (all-to-all) or the row stores (contiguous) when
+    // the kind is automatic, and are refused when bulk stores were asked for.
+    // The automatic all-to-all kind also takes whole-line row stores instead
+    // of row stores there, which such links drain far faster.
     const int dev_rc = outputs_in_device_memory(a2a, epi, shp);
     if (dev_rc < 0) return ATTN_A2A_ECUDA;
     if (dev_rc == 0) {

@@ -78,12 +78,12 @@ typedef struct {
   int store_kind;       /* how the tile owner stores its output tile:
                            0 = automatic: 1 for the contiguous layout and for the
                                all-to-all layout with P <= 8 and S <= 32768 (where
-                               it measured faster), else 2; where 1 would be chosen
-                               but an output buffer is not memory of the current
-                               device (cudaPointerGetAttributes: host memory the
-                               device can address, managed memory, another
-                               device's memory), 3 for the all-to-all layout and 2
-                               for the contiguous one;
+                               it measured faster), else 2; where an output buffer
+                               is not memory of the current device
+                               (cudaPointerGetAttributes: host memory the device
+                               can address, managed memory, another device's
+                               memory), 3 for the all-to-all layout, and 2 for the
+                               contiguous one;
                            1 = bulk tensor stores (TMA) from a shared-memory staging
                                tile: the owner commits the bulk group and resumes,
                                waiting only until the stores have read the staging
@@ -107,8 +107,8 @@ typedef struct {
                                made for the device's own memory, and is refused
                                there; 2 stores 16-byte pieces of 32 rows at a time,
                                which such links drain far more slowly). Chosen
-                               automatically only in place of 1 for outputs outside
-                               the device's memory.
+                               automatically for all-to-all outputs outside the
+                               device's memory.
                            Results are identical; values > 3 are ATTN_A2A_EINVAL */
   int grid;             /* persistent CTAs; 0 = one per SM */
   long long timeout_ns; /* limit of every in-kernel wait; 0 = 2 000 000 000 ns */

@@ -36,6 +36,7 @@ EXPORTED = (
     "attn_a2a_strerror",
     "attn_a2a_num_sms",
     "attn_a2a_store_kind",
+    "attn_a2a_split_plan",
 )
 
 
@@ -116,6 +117,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.attn_a2a_strerror.restype = ctypes.c_char_p
     lib.attn_a2a_num_sms.argtypes = []
     lib.attn_a2a_store_kind.argtypes = [cint, cint, cint, cint, ctypes.POINTER(ctypes.c_int)]
+    ip = ctypes.POINTER(ctypes.c_int)
+    lib.attn_a2a_split_plan.argtypes = [cint, cint, cint, cint, cint, cint, ctypes.c_longlong, cint, ip, ip, ip]
     for name in EXPORTED:
         if name != "attn_a2a_strerror":
             getattr(lib, name).restype = cint
@@ -365,6 +368,17 @@ def attn_a2a_strerror(code: int) -> str:
 
 def attn_a2a_num_sms() -> int:
     return num_sms()
+
+
+def attn_a2a_split_plan(B: int, H: int, S: int, d: int, grid: int = 0, split: int = SPLIT_AUTO, num_sms: int = 0,
+                        l2_bytes: int = 0):
+    """The split schedule a call with a workspace would use: (kind, first item, key blocks per
+    CTA range); kind SPLIT_ALL, SPLIT_TAIL or 0. num_sms / l2_bytes 0 = the current device's."""
+    kind, first, blocks = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
+    rc = load().attn_a2a_split_plan(int(B), int(H), int(S), int(d), int(grid), int(num_sms), int(l2_bytes),
+                                    int(split), ctypes.byref(kind), ctypes.byref(first), ctypes.byref(blocks))
+    _check(rc, "attn_a2a_split_plan", True)
+    return kind.value, first.value, blocks.value
 
 
 def attn_a2a_store_kind(S: int, P: int, layout: int, store_kind: int = 0) -> int:

@@ -7,6 +7,8 @@
 #include <cstring>
 #include <mutex>
 
+#include <climits>
+
 #include "attn_a2a.h"
 #include "internal.h"
 
@@ -269,6 +271,27 @@ const char* attn_a2a_strerror(int status) {
 }
 
 int attn_a2a_num_sms(void) { return num_sms_current_device(); }
+
+int attn_a2a_split_plan(int B, int H, int S, int d, int grid, int num_sms, long long l2_bytes, int split,
+                        int* kind, int* first_item, int* range_blocks) {
+  if (kind == nullptr || first_item == nullptr || range_blocks == nullptr || B < 0 || H < 0 || S < 0 ||
+      (d != 64 && d != 128) || grid < 0 || num_sms < 0 || l2_bytes < 0 || split < ATTN_A2A_SPLIT_AUTO ||
+      split > ATTN_A2A_SPLIT_NONE)
+    return ATTN_A2A_EINVAL;
+  const int nblk = (S + 127) / 128;
+  const long long total = static_cast<long long>(B) * H * ((nblk + 1) / 2);
+  if (total > INT_MAX) return ATTN_A2A_EUNSUPPORTED;
+  if (num_sms == 0) num_sms = num_sms_current_device();
+  if (l2_bytes == 0) l2_bytes = l2_bytes_current_device();
+  if (num_sms <= 0) return ATTN_A2A_ECUDA;
+  int g = grid > 0 ? grid : num_sms;
+  if (g > total) g = static_cast<int>(total);
+  int first = 0, len = 0;
+  *kind = split_decision(static_cast<int>(total), nblk, g, num_sms, 4LL * B * H * S * d, l2_bytes, split, first, len);
+  *first_item = first;
+  *range_blocks = len;
+  return ATTN_A2A_OK;
+}
 
 int attn_a2a_store_kind(int S, int P, int layout, int store_kind, int* resolved) {
   if (resolved == nullptr || S < 0 || P < 1 || P > kMaxRanks || layout < 0 || layout > 1 || store_kind < 0 ||

@@ -155,6 +155,39 @@ constexpr int kSplitMinSavedBlocks = 32;
 // the joint preset (5 of 108) 1.5 % faster.
 constexpr int kSplitAllMinSavedBlocks = 4;
 
+}  // namespace
+
+// The split decision for `total` work items of `nblk` key blocks on `grid`
+// CTAs of a GPU with num_sms SMs and l2_bytes of L2, kv_bytes the K and V
+// bytes of every head (the rule described at plan_split_tail):
+// ATTN_A2A_SPLIT_ALL or ATTN_A2A_SPLIT_TAIL with the first split item and the
+// blocks per range, or 0 (nothing split: tail_first = total, tail_len = 0).
+int split_decision(int total, int nblk, int grid, int num_sms, long long kv_bytes, long long l2_bytes, int split,
+                   int& tail_first, int& tail_len) {
+  tail_first = total;
+  tail_len = 0;
+  if (split == ATTN_A2A_SPLIT_NONE || total <= 0 || grid <= 0 || nblk < 2 || nblk > (1 << 20)) return 0;
+  const long long blocks = static_cast<long long>(total) * nblk;
+  if (blocks > INT_MAX / 2 || grid > num_sms) return 0;  // every range's CTA must be resident at once
+  const int waves = (total + grid - 1) / grid;
+  const int all_len = static_cast<int>((blocks + grid - 1) / grid);
+  const bool all_pays = 2 * kv_bytes <= l2_bytes && waves * nblk - all_len >= kSplitAllMinSavedBlocks;
+  if (split == ATTN_A2A_SPLIT_ALL || (split == ATTN_A2A_SPLIT_AUTO && all_pays)) {
+    tail_first = 0;
+    tail_len = all_len;
+    return ATTN_A2A_SPLIT_ALL;
+  }
+  const int r = total - (waves - 1) * grid;
+  if (r >= grid) return 0;  // the last wave is full
+  const int len = static_cast<int>((static_cast<long long>(r) * nblk + grid - 1) / grid);
+  if (split == ATTN_A2A_SPLIT_AUTO && nblk - len < kSplitMinSavedBlocks) return 0;
+  tail_first = (waves - 1) * grid;
+  tail_len = len;
+  return ATTN_A2A_SPLIT_TAIL;
+}
+
+namespace {
+
 // Split schedule (the kernel's tail_piece), with the caller's workspace:
 // ATTN_A2A_SPLIT_TAIL divides a last wave of r < grid items into ranges of
 // ceil(r * nblk / grid) <= nblk key blocks, one per CTA, run by a second
@@ -172,26 +205,11 @@ int plan_split_tail(tc::Params& p, int grid, int d, const attn_a2a_opts& opts, b
   whole = false;
   if (opts.workspace == nullptr || opts.split == ATTN_A2A_SPLIT_NONE) return ATTN_A2A_OK;
   if (opts.workspace_bytes < ATTN_A2A_WORKSPACE_BYTES(grid, d)) return ATTN_A2A_EINVAL;
-  if (opts.trace != nullptr || p.interleave > 1 || p.nblk < 2 || p.nblk > (1 << 20)) return ATTN_A2A_OK;
-  const long long blocks = static_cast<long long>(p.total) * p.nblk;
-  if (blocks > INT_MAX / 2 || grid > num_sms_current_device()) return ATTN_A2A_OK;
-  const int waves = (p.total + grid - 1) / grid;
-  const int all_len = static_cast<int>((blocks + grid - 1) / grid);
-  const long long kv_bytes = 4LL * p.B * p.H * p.S * d;  // bf16 K and V of every head
-  const bool all_pays = 2 * kv_bytes <= l2_bytes_current_device() &&
-                        waves * p.nblk - all_len >= kSplitAllMinSavedBlocks;
-  if (opts.split == ATTN_A2A_SPLIT_ALL || (opts.split == ATTN_A2A_SPLIT_AUTO && all_pays)) {
-    p.tail_first = 0;
-    p.tail_len = all_len;
-    whole = true;
-  } else {
-    const int r = p.total - (waves - 1) * grid;
-    if (r >= grid) return ATTN_A2A_OK;  // the last wave is full
-    const int len = static_cast<int>((static_cast<long long>(r) * p.nblk + grid - 1) / grid);
-    if (opts.split == ATTN_A2A_SPLIT_AUTO && p.nblk - len < kSplitMinSavedBlocks) return ATTN_A2A_OK;
-    p.tail_first = (waves - 1) * grid;
-    p.tail_len = len;
-  }
+  if (opts.trace != nullptr || p.interleave > 1) return ATTN_A2A_OK;
+  const int kind = split_decision(p.total, p.nblk, grid, num_sms_current_device(), 4LL * p.B * p.H * p.S * d,
+                                  l2_bytes_current_device(), opts.split, p.tail_first, p.tail_len);
+  if (kind == 0) return ATTN_A2A_OK;
+  whole = kind == ATTN_A2A_SPLIT_ALL;
   uint8_t* base = static_cast<uint8_t*>(opts.workspace);
   const size_t flags = (static_cast<size_t>(grid) * 32u + 255u) / 256u * 256u;
   p.ws_flags = reinterpret_cast<unsigned*>(base);

@@ -23,6 +23,10 @@ long long l2_bytes_current_device();
 // built (the all-to-all layout with P > 8). store_kind 0 picks what measured
 // faster; it must be 0, 1 or 2.
 int resolve_store_kind(int S, int P, bool a2a, int store_kind);
+// The split schedule's decision (see fa_tc.cu): ATTN_A2A_SPLIT_ALL,
+// ATTN_A2A_SPLIT_TAIL or 0, with the first split item and blocks per range.
+int split_decision(int total, int nblk, int grid, int num_sms, long long kv_bytes, long long l2_bytes, int split,
+                   int& tail_first, int& tail_len);
 
 int launch_fa_tc(const void* q, const void* k, const void* v, const attn_a2a_shape& shp,
                  float scale, bool a2a, const EpiParams& epi, int* dev_status,

@@ -198,21 +198,10 @@ def measure(cfg, R: float, n_sm: int, trace: bool = True) -> dict:
 
 
 def split_kind(cfg, n_sm: int):
-    """The split the library picks automatically for cfg with a workspace (its
-    rule restated): "all", "tail" or None."""
-    nblk = (cfg.S + 127) // 128
-    total = cfg.B * cfg.H * ((nblk + 1) // 2)
-    grid = min(n_sm, total)
-    if nblk < 2:
-        return None
-    waves = (total + grid - 1) // grid
-    l2 = torch.cuda.get_device_properties(0).L2_cache_size
-    if 2 * 4 * cfg.B * cfg.H * cfg.S * cfg.d <= l2 and waves * nblk - (total * nblk + grid - 1) // grid >= 4:
-        return "all"
-    r = total - (waves - 1) * grid
-    if r < grid and nblk - (r * nblk + grid - 1) // grid >= 32:
-        return "tail"
-    return None
+    """The split the library picks automatically for cfg with a workspace
+    (attn_a2a_split_plan): "all", "tail" or None."""
+    kind, _, _ = bd.attn_a2a_split_plan(cfg.B, cfg.H, cfg.S, cfg.d, grid=n_sm)
+    return {bd.SPLIT_ALL: "all", bd.SPLIT_TAIL: "tail"}.get(kind)
 
 
 def report(H=40, d=128, P=8, s_list=S_LIST, presets=PRESETS, quick=False) -> dict:

@@ -45,29 +45,14 @@ KERNEL_SOURCES = ["fa_tc.cuh", "ptx.cuh", "epilogue.cuh", "tmem_ops.cuh", "fa_tc
                   "fa_tc_split.cu"]
 
 
-def split_plan(cfg, grid: int, l2_bytes: int):
-    """How a call with a workspace and the automatic split divides cfg's work items (the
-    launcher's rule): "all" (every item's key blocks in equal ranges, one kernel), "tail"
-    (the partial last wave's, in a second kernel) or None."""
-    nblk = (cfg.S + 127) // 128
-    total = cfg.B * cfg.H * ((nblk + 1) // 2)
-    grid = min(grid, total)
-    if nblk < 2:
-        return None
-    waves = (total + grid - 1) // grid
-    if 2 * 4 * cfg.B * cfg.H * cfg.S * cfg.d <= l2_bytes and waves * nblk - (total * nblk + grid - 1) // grid >= 4:
-        return "all"
-    r = total - (waves - 1) * grid
-    if r < grid and nblk - (r * nblk + grid - 1) // grid >= 32:
-        return "tail"
-    return None
-
-
 def device_split_plan(cfg):
-    import torch
+    """How a call with a workspace and the automatic split divides cfg's work items on this
+    GPU (the library's own decision, attn_a2a_split_plan): "all" (every item's key blocks in
+    equal ranges, one kernel), "tail" (the partial last wave's, in a second kernel) or None."""
     from attention_all_layout_gb300 import binding as bd
 
-    return split_plan(cfg, bd.num_sms(), torch.cuda.get_device_properties(0).L2_cache_size)
+    kind, _, _ = bd.attn_a2a_split_plan(cfg.B, cfg.H, cfg.S, cfg.d)
+    return {bd.SPLIT_ALL: "all", bd.SPLIT_TAIL: "tail"}.get(kind)
 
 
 def fused_kernel_label(cfg, split: bool) -> str:

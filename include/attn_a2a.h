@@ -446,6 +446,22 @@ int attn_a2a_num_sms(void);
  * range. Host-only, no launch. */
 int attn_a2a_store_kind(int S, int P, int layout, int store_kind, int* resolved);
 
+/* The split schedule (attn_a2a_opts.split, with a large enough workspace) an
+ * attn_a2a_fwd_ex or attn_a2a_fwd_contig_ex call of B x H heads of length S,
+ * head dimension d, would use on `grid` persistent CTAs (0 = one per SM) of a
+ * GPU with num_sms SMs and l2_bytes of L2 (0 = those of the current device):
+ * writes *kind = ATTN_A2A_SPLIT_ALL (every work item's key blocks in equal
+ * ranges, one per CTA), ATTN_A2A_SPLIT_TAIL (the partial last wave's, in a
+ * second kernel) or 0 (nothing split), *first_item = the first split work item
+ * and *range_blocks = the key blocks per CTA range (0 when nothing is split).
+ * Work items are pairs of 128-row query tiles, B*H*ceil(ceil(S/128)/2) of
+ * them. Not split either way: trace calls and tile_order = 1. Returns
+ * ATTN_A2A_OK; ATTN_A2A_EINVAL for arguments out of range (d other than 64 or
+ * 128); ATTN_A2A_ECUDA if 0 asks for a device value and there is no device.
+ * Host-only, no launch. */
+int attn_a2a_split_plan(int B, int H, int S, int d, int grid, int num_sms, long long l2_bytes, int split,
+                        int* kind, int* first_item, int* range_blocks);
+
 #ifdef __cplusplus
 }
 #endif

@@ -118,6 +118,24 @@ def test_store_kind_query(lib):
     assert lib.attn_a2a_store_kind(4096, 8, 1, 0, None) == bd.EINVAL
 
 
+def test_split_plan_query(lib):
+    L2 = 126 * 2**20
+    # image: the whole schedule in 81-block ranges; video: the last wave in 176-block ranges;
+    # H = 40, S = 4096 (K and V beyond half of L2, tail saves too little): nothing
+    assert bd.attn_a2a_split_plan(1, 24, 4096, 128, num_sms=152, l2_bytes=L2) == (bd.SPLIT_ALL, 0, 81)
+    assert bd.attn_a2a_split_plan(1, 40, 32768, 128, num_sms=152, l2_bytes=L2) == (bd.SPLIT_TAIL, 5016, 176)
+    assert bd.attn_a2a_split_plan(1, 40, 4096, 128, num_sms=152, l2_bytes=L2)[0] == 0
+    assert bd.attn_a2a_split_plan(1, 24, 4096, 128, split=bd.SPLIT_NONE, num_sms=152, l2_bytes=L2)[0] == 0
+    # a grid larger than the SM count is never split (its CTAs need not all be resident)
+    assert bd.attn_a2a_split_plan(1, 24, 4096, 128, grid=200, num_sms=152, l2_bytes=L2)[0] == 0
+    out = [ctypes.c_int(0) for _ in range(3)]
+    ptrs = [ctypes.byref(x) for x in out]
+    for args in ((1, 24, 4096, 96, 0, 152, L2, 0), (1, 24, 4096, 128, -1, 152, L2, 0),
+                 (1, 24, 4096, 128, 0, 152, L2, 4), (-1, 24, 4096, 128, 0, 152, L2, 0)):
+        assert lib.attn_a2a_split_plan(*args, *ptrs) == bd.EINVAL
+    assert lib.attn_a2a_split_plan(1, 24, 4096, 128, 0, 152, L2, 0, None, ptrs[1], ptrs[2]) == bd.EINVAL
+
+
 def test_empty_problem_is_ok_without_launch(lib):
     # S = 0: every chunk is empty, null partitions are allowed, nothing is launched
     assert call_fwd(lib, S=0, parts=[0, 0]) == bd.OK

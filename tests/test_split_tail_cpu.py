@@ -151,3 +151,29 @@ def test_split_shapes_of_the_presets():
     assert plan(304, 152, 32) == (304, 0, False)
     assert plan(304, 152, 32, TAIL) == (304, 0, False)
     assert plan(304, 152, 32, NONE) == (304, 0, False)
+
+
+# The library's own decision (attn_a2a_split_plan, host-only) against the
+# restatement above, for whole problems (B x H heads of length S) on a GPU of
+# 152 SMs and a GB300-sized L2.
+PROBLEMS = [(1, 24, 4096), (1, 24, 4608), (1, 40, 32768), (1, 40, 75600), (1, 40, 4096), (2, 3, 5000),
+            (1, 4, 8192), (1, 2, 8192), (1, 3, 8320), (1, 1, 256), (3, 7, 1000), (1, 8, 16384)]
+
+
+@pytest.mark.parametrize("B,H,S", PROBLEMS)
+@pytest.mark.parametrize("grid", [0, 24, 100])
+@pytest.mark.parametrize("split", [AUTO, TAIL, ALL, NONE])
+def test_library_plan_matches_restatement(B, H, S, grid, split):
+    bd = pytest.importorskip("attention_all_layout_gb300.binding")
+    try:
+        bd.load()
+    except Exception as e:  # the library must have been built for this test
+        pytest.skip(f"library not loadable: {e}")
+    d, n_sm = 128, 152
+    nblk = (S + 127) // 128
+    total = B * H * ((nblk + 1) // 2)
+    g = min(grid or n_sm, total)
+    first, length, whole = plan(total, g, nblk, split, kv_bytes=kv(B, H, S, d), l2=L2)
+    kind, c_first, c_len = bd.attn_a2a_split_plan(B, H, S, d, grid, split, num_sms=n_sm, l2_bytes=L2)
+    want_kind = 0 if first >= total else (ALL if whole else TAIL)
+    assert (kind, c_first if kind else total, c_len) == (want_kind, first, length)

@@ -16,7 +16,8 @@
 //   warp 2      relay: waits on the TMA and O-free barriers on the issuer's
 //               behalf; with the softmax threads' own arrivals it completes
 //               one event barrier phase per group of MMAs
-//   warp 3      idle
+//   warp 3      bulk-store modes: issues the output tiles' tensor stores
+//               (store_role); otherwise idle
 //   warps 4-7   softmax/correction/epilogue for query tile 0 (128 rows)
 //   warps 8-11  the same for query tile 1
 // A work item is (b, h, pair of adjacent 128-row query blocks), so each K/V
@@ -68,7 +69,7 @@ constexpr uint32_t kTmemCols = 512;
 // maximum is taken and O and l are rescaled.
 constexpr float kSpecBound = 4096.0f;  // 2^12
 // Register split (setmaxnreg): the kernel launches with kLaunchRegs per thread;
-// warpgroup 0 (producer, MMA issuer, relay, one idle warp) gives registers back and
+// warpgroup 0 (producer, MMA issuer, relay, store warp) gives registers back and
 // the two softmax warpgroups take them: 128*kRegsLow + 256*kRegsHigh must not
 // exceed 384*kLaunchRegs, else setmaxnreg.inc would wait forever. The launcher
 // refuses to launch unless the compiled launch register count is kLaunchRegs.
@@ -123,8 +124,9 @@ struct Cfg {
 //                partitions; only a partition's last block can be partial.
 //   kModeA2AT    as kModeA2A, but each output tile goes out as bulk tensor
 //                stores (TMA) from a shared-memory staging buffer: the owner
-//                commits the bulk group and resumes; only the buffer's reuse
-//                waits, for the stores' shared-memory reads. A tile that
+//                warps stage the tile and resume; one thread of warp 3 issues
+//                the tile's stores, and only the buffer's reuse waits, for the
+//                stores' shared-memory reads. A tile that
 //                straddles two partitions is stored row by row as in kModeA2A.
 //   kModeContigT as kModeContig, with the bulk-store epilogue.
 //   kModeS2SG    as kModeS2S (sequence-sharded in and out), for partitions of
@@ -662,20 +664,12 @@ __device__ __forceinline__ float probs(const uint32_t (&sr)[128], uint32_t (&pk)
   return s0 + s1;
 }
 
-// Bulk-store epilogue of one tile (kModeA2AT, kModeS2SGT): the 128 owner threads write
-// their normalised bf16 rows into the staging buffer (128-byte swizzle, as
-// the tensor map expects), hand them to the async proxy, and one elected
-// thread issues the tile's tensor stores through output map `map` at
-// coordinates (column, y, z, batch) - (head, first row) for a partition,
-// (first row, head) for the contiguous layout - commits the bulk group, waits
-// only until the buffer has been read, and passes the buffer on. Returns
-// false on abort.
-template <int D, int NMAP>
-__device__ __forceinline__ bool bulk_store_tile(const Maps<NMAP>* maps, uint32_t stg, uint32_t bar_stg,
-                                                uint32_t bar_stgw, uint32_t stg_parity, uint32_t stgw_parity,
-                                                bool wait_stg, int r, int lane, bool elected, const uint32_t (&o)[D],
-                                                float inv_l, int map, int y, int z, int b, const WaitCtl& w) {
-  if (wait_stg && !__all_sync(0xffffffffu, mbar_wait(bar_stg, stg_parity, w))) return false;
+// Bulk-store epilogue of one tile (kModeA2AT, kModeContigT, kModeS2SGT), the
+// owner threads' part: each writes its normalised bf16 row into the staging
+// buffer (128-byte swizzle, as the tensor map expects) and hands it to the
+// async proxy. The store role issues the tile's tensor stores.
+template <int D>
+__device__ __forceinline__ void stage_tile(uint32_t stg, int r, const uint32_t (&o)[D], float inv_l) {
 #pragma unroll
   for (int c = 0; c < D / 8; ++c) {
     const uint32_t a = static_cast<uint32_t>(c / 8) * (128u * 128u);  // 64-column atom
@@ -687,17 +681,70 @@ __device__ __forceinline__ bool bulk_store_tile(const Maps<NMAP>* maps, uint32_t
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(x), "r"(y), "r"(z), "r"(v) : "memory");
   }
   fence_proxy_async_smem();
-  __syncwarp();
-  if (lane == 0) mbar_arrive(bar_stgw);
-  if (elected) {
-    if (!mbar_wait(bar_stgw, stgw_parity, w)) return false;
-#pragma unroll
-    for (int a = 0; a < D / 64; ++a) tma_store_4d(&maps->o[map], stg + a * 128 * 128, a * 64, y, z, b);
-    bulk_commit_group();
-    bulk_wait_read_all();  // the buffer may be reused once the stores have read it
-    mbar_arrive(bar_stg);
+}
+
+// Where tile t of work item wi goes by bulk tensor store: false when the tile
+// has no rows or straddles two partitions (then its rows are stored from
+// registers); else the output map and the coordinates (y, z) - (head, first
+// row in the partition) for the all-to-all layout, (first row, head) for the
+// contiguous one.
+template <int MODE>
+__device__ __forceinline__ bool tile_store_target(const Params& p, const Item& wi, int t, int& map, int& y, int& z) {
+  const int s0 = (2 * wi.pair + t) * kBM;  // the tile's first sequence row
+  map = 0;
+  if (s0 >= p.S) return false;
+  if constexpr (MODE == kModeContigT) {
+    y = s0;
+    z = wi.h;
+    return true;
+  } else {
+    int j0, l0, c0, j1, l1, c1;
+    chunk_of_row(p.epi, s0, j0, l0, c0);
+    chunk_of_row(p.epi, min(s0 + kBM, p.S) - 1, j1, l1, c1);
+    map = j0;
+    y = wi.h;
+    z = l0;
+    return j0 == j1 && j0 < kMaxStoreMaps;  // the whole tile lands in one partition
   }
-  return true;
+}
+
+// ------------------------------------------------------------------ store role
+// Bulk-store modes: one thread of warp 3 issues every tile's tensor stores, so
+// that the owner warps go back to their next work as soon as they have staged
+// their rows. Epilogue uses are numbered u = 2 it + t (tile 0, then tile 1, of
+// each piece); for every use, bulk or not, it waits until the four owner warps
+// have arrived on STGW + t (after staging, or at once for a tile without bulk
+// stores or a partial piece's), issues the tile's stores and waits until they
+// have read the staging buffer, and then releases the buffer to use u + 1
+// (token STG, one phase per use). The owners of use u wait for that release of
+// use u - 1 before they arrive, so neither side gets more than one use ahead.
+// Before returning (also on an abort) it waits until its stores have completed.
+template <int D, int MODE, int NMAP, bool SPLIT>
+__device__ void store_role(const Params& p, const Maps<NMAP>* maps, uint32_t stg, uint32_t bar0, const WaitCtl& w) {
+  using C = Cfg<D>;
+  auto BAR = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
+  uint32_t n[2] = {0, 0};  // uses of each tile so far
+  bool ok = true;
+  for (int it = 0; ok; ++it) {
+    Piece pc;
+    if (!piece_at<SPLIT>(p, it, pc)) break;
+    const Item wi = decode_item(p, pc.item);
+    for (int t = 0; t < 2; ++t) {
+      if (!mbar_wait(BAR(C::STGW + t), n[t]++ & 1u, w)) {
+        ok = false;
+        break;
+      }
+      int map, y, z;
+      if (!(SPLIT && pc.kind == 1) && tile_store_target<MODE>(p, wi, t, map, y, z)) {
+#pragma unroll
+        for (int a = 0; a < D / 64; ++a) tma_store_4d(&maps->o[map], stg + a * 128 * 128, a * 64, y, z, wi.b);
+        bulk_commit_group();
+        bulk_wait_read_all();  // the buffer may be reused once the stores have read it
+      }
+      mbar_arrive(BAR(C::STG));
+    }
+  }
+  bulk_wait_all();
 }
 
 // Partial piece of a split item: this thread's row of the tile - unnormalised
@@ -827,7 +874,6 @@ __device__ void softmax_role(const Params& p, int t, uint32_t bar0, uint32_t tme
   const uint32_t tO = tmem + lane_off + 256 + t * D;
   const float sl2 = p.scale_log2;
   uint32_t sf_cnt = 0;
-  uint32_t stgw_cnt = 0;  // this tile's bulk stores so far (phases of STGW + t)
   for (int it = 0;; ++it) {
     int item, nb;
     {
@@ -938,10 +984,11 @@ __device__ void softmax_role(const Params& p, int t, uint32_t bar0, uint32_t tme
         tc_fence_before();
         mbar_arrive(BAR(C::OE + t));
         if constexpr (kBulkStores<MODE>) {
+          // no stores for the store role: this use only passes the staging buffer on
           const uint32_t u = 2u * static_cast<uint32_t>(it) + static_cast<uint32_t>(t);
-          if ((warp & 3) == 0 && lane == 0) {
+          if (lane == 0) {
             if (u > 0 && !mbar_wait(BAR(C::STG), (u - 1) & 1u, w)) return;
-            mbar_arrive(BAR(C::STG));
+            mbar_arrive(BAR(C::STGW + t));
           }
         }
         continue;
@@ -958,38 +1005,25 @@ __device__ void softmax_role(const Params& p, int t, uint32_t bar0, uint32_t tme
       tr_c0 = clock64();
     }
     if constexpr (kBulkStores<MODE>) {
-      // Epilogue uses are numbered u = 2 it + t; use u waits until use u - 1
-      // has released the staging buffer (token STG, one phase per use).
+      // Epilogue uses are numbered u = 2 it + t; use u waits until the store
+      // role has released the staging buffer after use u - 1 (token STG, one
+      // phase per use), stages the tile when it goes out by bulk stores, and
+      // each warp arrives on STGW + t for the store role, which issues them.
       const uint32_t u = 2u * static_cast<uint32_t>(it) + static_cast<uint32_t>(t);
-      const bool elected = (warp & 3) == 0 && lane == 0;
-      bool bulk = false;
-      int map = 0, y = 0, z = 0;
-      const int s0 = (2 * wi.pair + t) * kBM;  // the tile's first sequence row
-      if constexpr (MODE == kModeContigT) {
-        bulk = s0 < p.S;
-        y = s0;
-        z = wi.h;
-      } else if (s0 < p.S) {
-        int j0, l0, c0, j1, l1, c1;
-        chunk_of_row(p.epi, s0, j0, l0, c0);
-        chunk_of_row(p.epi, min(s0 + kBM, p.S) - 1, j1, l1, c1);
-        bulk = j0 == j1 && j0 < kMaxStoreMaps;  // the whole tile lands in one partition
-        map = j0;
-        y = wi.h;
-        z = l0;
-      }
+      int map, y, z;
+      const bool bulk = tile_store_target<MODE>(p, wi, t, map, y, z);
       if (bulk) {
-        if (!bulk_store_tile<D, NMAP>(maps, stg, BAR(C::STG), BAR(C::STGW + t), (u - 1) & 1u, stgw_cnt & 1u,
-                                      u > 0, r, lane, elected, o, 1.0f / l, map, y, z, wi.b, w))
-          return;
-        ++stgw_cnt;
+        if (u > 0 && !__all_sync(0xffffffffu, mbar_wait(BAR(C::STG), (u - 1) & 1u, w))) return;
+        stage_tile<D>(stg, r, o, 1.0f / l);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(BAR(C::STGW + t));
         trace_out();
         continue;
       }
-      // no bulk store for this tile: pass the buffer on in turn
-      if (elected) {
+      // no bulk store for this tile: its rows go from registers below
+      if (lane == 0) {
         if (u > 0 && !mbar_wait(BAR(C::STG), (u - 1) & 1u, w)) return;
-        mbar_arrive(BAR(C::STG));
+        mbar_arrive(BAR(C::STGW + t));
       }
     }
     uint16_t* dst = nullptr;
@@ -1109,12 +1143,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mma_role<D, SPLIT>(p, sbase, bar0, tmem, w);
     } else if (warp == 2) {
       if (lane == 0) relay_role<D, SPLIT>(p, bar0, w);
+    } else if constexpr (kBulkStores<MODE>) {
+      // every bulk store has completed before the store role returns
+      if (lane == 0) store_role<D, MODE, NMAP, SPLIT>(p, &maps, sbase + C::STG_OFF, bar0, w);
     }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
     softmax_role<D, MODE, NMAP, TRACE, SPLIT>(p, (warp - 4) / 4, bar0, tmem, &maps, sbase + C::STG_OFF, w);
-    // the bulk-store issuers: every store must have completed before the CTA exits
-    if (kBulkStores<MODE> && (warp & 3) == 0 && lane == 0) bulk_wait_all();
   }
   tc_fence_before();
   __syncthreads();

@@ -17,12 +17,13 @@ namespace attn_a2a {
 namespace {
 
 // Longest sequence, in 128-row key blocks, for which the automatic store kind
-// picks bulk tensor stores for the all-to-all layout (S <= 32768). Measured
-// at H = 40, d = 128, P = 8 on the current kernel (bulk / row stores, calls
-// alternating, median of pairs): S = 24576 0.988, 32768 0.993 (bench-length
-// turns: 13.70 against 13.79 ms), 75600 1.003. (The first kernel measured
-// 1.008 at 24576 and 1.004 at 32768, when the boundary was S = 16384.)
-constexpr int kBulkA2AMaxBlocks = 256;
+// picks bulk tensor stores for the all-to-all layout: every length. Measured
+// at H = 40, d = 128, P = 8 with the current kernel, where warp 3 issues the
+// stores (bulk / row stores, calls alternating, median of pairs): S = 32768
+// 0.979, 49152 0.978, 75600 0.989. (Before the store warp: 0.988 at 24576,
+// 0.993 at 32768, 1.003 at 75600, and the boundary was S = 32768; with the
+// first kernel 1.008 at 24576, 1.004 at 32768, and it was S = 16384.)
+constexpr int kBulkA2AMaxBlocks = INT_MAX;
 // The same boundary for the whole Ulysses layer (sequence-sharded inputs):
 // there bulk stores also mean tiles counted over the whole sequence
 // (kModeS2SGT), measured against the per-partition tiles of kModeS2S only up

@@ -77,8 +77,8 @@ typedef struct {
 typedef struct {
   int store_kind;       /* how the tile owner stores its output tile:
                            0 = automatic: 1 for the contiguous layout and for the
-                               all-to-all layout with P <= 8 and S <= 32768 (where
-                               it measured faster), else 2; where an output buffer
+                               all-to-all layout with P <= 8 (where it measured
+                               faster), else 2; where an output buffer
                                is not memory of the current device
                                (cudaPointerGetAttributes: host memory the device
                                can address, managed memory, another device's

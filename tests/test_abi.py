@@ -98,11 +98,11 @@ def test_bad_options_rejected(lib):
 
 def test_store_kind_query(lib):
     # the automatic kind: bulk tensor stores for the contiguous layout, and for
-    # the all-to-all layout with P <= 8 up to 256 key blocks (S = 32768)
+    # the all-to-all layout with P <= 8, at every length
     assert bd.attn_a2a_store_kind(32768, 1, 0) == 1
     assert bd.attn_a2a_store_kind(32768, 8, 1) == 1
-    assert bd.attn_a2a_store_kind(32769, 8, 1) == 2
-    assert bd.attn_a2a_store_kind(75600, 8, 1) == 2
+    assert bd.attn_a2a_store_kind(32769, 8, 1) == 1
+    assert bd.attn_a2a_store_kind(75600, 8, 1) == 1
     assert bd.attn_a2a_store_kind(4096, 16, 1) == 2
     assert bd.attn_a2a_store_kind(0, 2, 1) == 1
     # an explicit kind is kept where it is built

@@ -89,9 +89,8 @@ def test_line_stores_traced():
 @pytest.mark.parametrize("name", ["small", "image", "long"])
 @pytest.mark.parametrize("store_kind", [0, 2, 3])
 def test_partitions_in_host_memory(name, store_kind):
-    # kind 0 (automatic) would take bulk stores (small, image) or row stores
-    # (long: S > 32768) for device partitions; for host partitions the library
-    # takes the whole-line row stores
+    # kind 0 (automatic) would take bulk stores for device partitions; for host
+    # partitions the library takes the whole-line row stores
     cfg = {"small": workloads.AttnConfig("host", B=1, H=3, S=1000, d=128, P=3), "image": workloads.CONFIGS["image"],
            "long": workloads.AttnConfig("host", B=1, H=2, S=33000, d=64, P=2)}[name]
     q, k, v = workloads.make_qkv(cfg, seed=9, device="cuda")

@@ -250,9 +250,9 @@ def test_bulk_store_epilogue_matches_register_stores(case):
 
 
 @pytest.mark.parametrize("S", [16384, 32768, 32769])
-def test_automatic_store_kind_around_its_switch(S):
-    # the automatic kind takes bulk stores up to 256 key blocks (S = 32768)
-    # and row stores above; every kind writes the same bytes
+def test_automatic_store_kind_matches_both_kinds(S):
+    # the automatic kind (bulk stores at every length, where the partitions
+    # are device memory and P <= 8) and both explicit kinds write the same bytes
     cfg = workloads.AttnConfig(f"switch_{S}", B=1, H=2, S=S, d=128, P=2)
     _, _, _, dq, dk, dv = cuda_qkv(cfg, seed=14)
     outs = [fused(dq, dk, dv, cfg.P, cfg.scale, store_kind=kind) for kind in (0, 1, 2)]

@@ -152,9 +152,10 @@ constexpr int kSplitMinSavedBlocks = 32;
 // once, so with more K/V than L2 holds every range re-reads its heads' K and
 // V from HBM (measured on GB300: video and long presets 20 % slower). A cut
 // item costs a partial write (3.6 us) and a merge (2-3 us) on the critical
-// path: measured, the image preset (15 blocks saved of 96) ran 8.5 % faster,
-// the joint preset (5 of 108) 1.5 % faster.
-constexpr int kSplitAllMinSavedBlocks = 4;
+// path: measured with warp 3 issuing the bulk stores, the image preset (15
+// blocks saved of 96) ran 7 % faster split (0.144 against 0.154 ms), the
+// joint preset (5 of 108) no faster (0.178 against 0.177-0.179 ms).
+constexpr int kSplitAllMinSavedBlocks = 8;
 
 }  // namespace
 

@@ -123,6 +123,9 @@ def test_split_plan_query(lib):
     # image: the whole schedule in 81-block ranges; video: the last wave in 176-block ranges;
     # H = 40, S = 4096 (K and V beyond half of L2, tail saves too little): nothing
     assert bd.attn_a2a_split_plan(1, 24, 4096, 128, num_sms=152, l2_bytes=L2) == (bd.SPLIT_ALL, 0, 81)
+    # joint: 103-block ranges would save 5 of 108 key blocks per CTA, too few
+    assert bd.attn_a2a_split_plan(1, 24, 4608, 128, num_sms=152, l2_bytes=L2)[0] == 0
+    assert bd.attn_a2a_split_plan(1, 24, 4608, 128, split=bd.SPLIT_ALL, num_sms=152, l2_bytes=L2) == (bd.SPLIT_ALL, 0, 103)
     assert bd.attn_a2a_split_plan(1, 40, 32768, 128, num_sms=152, l2_bytes=L2) == (bd.SPLIT_TAIL, 5016, 176)
     assert bd.attn_a2a_split_plan(1, 40, 4096, 128, num_sms=152, l2_bytes=L2)[0] == 0
     assert bd.attn_a2a_split_plan(1, 24, 4096, 128, split=bd.SPLIT_NONE, num_sms=152, l2_bytes=L2)[0] == 0

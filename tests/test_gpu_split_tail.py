@@ -27,7 +27,7 @@ from gpu_helpers import REL_FRO, GuardedPartitions, abs_tolerance, rel_fro
 pytestmark = pytest.mark.gpu
 
 MIN_SAVED = 32  # key blocks per CTA the automatic tail split must save (the launcher's rule)
-MIN_SAVED_ALL = 4  # the same for the whole-schedule split, which needs K and V in half of L2
+MIN_SAVED_ALL = 8  # the same for the whole-schedule split, which needs K and V in half of L2
 
 # (B, H, S, d, P, grid); items = B * H * ceil(ceil(S/128)/2)
 CASES = [
@@ -184,16 +184,18 @@ def test_video_preset_split_tail_full_size():
 
 
 def test_automatic_choice_on_the_presets():
-    # image and joint: K and V fit in half of L2 and the whole-schedule split saves
-    # CTAs key blocks, so the automatic choice is SPLIT_ALL (the same bytes);
-    # SPLIT_NONE with a workspace is the call without one
-    for name in ("image", "joint"):
+    # image: K and V fit in half of L2 and the whole-schedule split saves CTAs 15
+    # key blocks, so the automatic choice is SPLIT_ALL (the same bytes); joint: it
+    # would save 5, too few, so the call is the unsplit one; SPLIT_NONE with a
+    # workspace is the call without one
+    for name, want in (("image", bd.SPLIT_ALL), ("joint", 0)):
         cfg = workloads.CONFIGS[name]
-        first, _, _, cut = geometry(cfg.B, cfg.H, cfg.S, bd.num_sms(), bd.SPLIT_AUTO, cfg.d)
-        assert first == 0 and cut
+        assert bd.attn_a2a_split_plan(cfg.B, cfg.H, cfg.S, cfg.d)[0] == want
+        first, _, total, cut = geometry(cfg.B, cfg.H, cfg.S, bd.num_sms(), bd.SPLIT_AUTO, cfg.d)
+        assert (first == 0 and cut) if want else first == total
         dq, dk, dv = (t.cuda() for t in workloads.make_qkv(cfg, seed=1))
         a = run_fused(dq, dk, dv, cfg, 0, bd.alloc_workspace(cfg.d), 0)
-        b = run_fused(dq, dk, dv, cfg, 0, bd.alloc_workspace(cfg.d), 0, bd.SPLIT_ALL)
+        b = run_fused(dq, dk, dv, cfg, 0, bd.alloc_workspace(cfg.d), 0, want or bd.SPLIT_NONE)
         assert_same_bytes(a.parts, b.parts)
         c = run_fused(dq, dk, dv, cfg, 0, bd.alloc_workspace(cfg.d), 0, bd.SPLIT_NONE)
         e = run_fused(dq, dk, dv, cfg, 0, None, 0)

@@ -13,9 +13,9 @@ split kinds (the last wave in a tail kernel; every item in one kernel):
   runs on a CTA of lower index than the final piece's - so a final piece waits
   only on pieces that wait on nothing, on CTAs dispatched no later;
 * the automatic choice takes the whole-schedule split where the K and V of
-  every head fit in half of L2 and it saves at least 4 key blocks per CTA (the
-  image and joint presets), else the last wave's split where that saves at
-  least 32 key blocks per CTA (video and long).
+  every head fit in half of L2 and it saves at least 8 key blocks per CTA (the
+  image preset), else the last wave's split where that saves at least 32 key
+  blocks per CTA (video and long); joint stays unsplit.
 """
 import pytest
 
@@ -32,7 +32,7 @@ def plan(total, grid, nblk, split=AUTO, min_saved=32, kv_bytes=1 << 40, l2=L2):
         return total, 0, False
     waves = (total + grid - 1) // grid
     all_len = (total * nblk + grid - 1) // grid
-    if split == ALL or (split == AUTO and 2 * kv_bytes <= l2 and waves * nblk - all_len >= 4):
+    if split == ALL or (split == AUTO and 2 * kv_bytes <= l2 and waves * nblk - all_len >= 8):
         return 0, all_len, True
     r = total - (waves - 1) * grid
     if r >= grid:
@@ -139,9 +139,10 @@ def test_split_shapes_of_the_presets():
     assert plan(384, 152, 32, kv_bytes=image) == (0, 81, True)
     assert plan(384, 152, 32, ALL) == (0, 81, True)
     assert plan(384, 152, 32, kv_bytes=image, l2=64 * 2**20) == (384, 0, False)  # a smaller L2: no split
-    # joint: 432 items of 36 blocks -> 128 in the last wave; 103-block ranges save 5 of 108
-    assert plan(432, 152, 36, kv_bytes=kv(1, 24, 4608, 128)) == (0, 103, True)
-    assert plan(432, 152, 36) == (432, 0, False)  # K and V beyond half of L2: no split
+    # joint: 432 items of 36 blocks -> 128 in the last wave; 103-block ranges would save
+    # 5 of 108, fewer than the 8 the automatic choice asks for: not split
+    assert plan(432, 152, 36, kv_bytes=kv(1, 24, 4608, 128)) == (432, 0, False)
+    assert plan(432, 152, 36, ALL) == (0, 103, True)
     # video: 5120 items of 256 blocks -> 104 in the last wave, 176-block ranges (80 saved);
     # K and V (671 MB) far beyond L2
     assert plan(5120, 152, 256, kv_bytes=kv(1, 40, 32768, 128)) == (5016, 176, False)

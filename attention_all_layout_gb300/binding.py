@@ -59,6 +59,7 @@ class Opts(ctypes.Structure):
         ("split", ctypes.c_int),
         ("workspace", ctypes.c_void_p),
         ("workspace_bytes", ctypes.c_longlong),
+        ("cta_pairs", ctypes.c_int),
     ]
 
 
@@ -195,13 +196,14 @@ def _ptr_array(tensors: Sequence):
 
 
 SPLIT_AUTO, SPLIT_TAIL, SPLIT_ALL, SPLIT_NONE = 0, 1, 2, 3  # attn_a2a_opts.split
+PAIRS_AUTO, PAIRS_ON, PAIRS_OFF = 0, 1, 2  # attn_a2a_opts.cta_pairs
 
 
 def _opts(store_kind=0, grid=0, timeout_ns=0, inject_stall=0, tile_order=0, trace=None, part_heads=0,
-          workspace=None, split=SPLIT_AUTO) -> Opts:
+          workspace=None, split=SPLIT_AUTO, cta_pairs=PAIRS_AUTO) -> Opts:
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     return Opts(store_kind, grid, timeout_ns, inject_stall, tile_order, _ptr(trace), part_heads, split,
-                _ptr(workspace), ws_bytes)
+                _ptr(workspace), ws_bytes, cta_pairs)
 
 
 def workspace_bytes(grid: int, d: int) -> int:
@@ -245,18 +247,21 @@ def _check(code: int, what: str, check: bool) -> int:
 def attn_a2a_fwd(q, k, v, P: int, scale: float, out_partitions, dev_status=None, stream=None,
                  store_kind: int = 0, grid: int = 0, timeout_ns: int = 0, inject_stall: int = 0,
                  tile_order: int = 0, trace=None, part_heads: int = 0, workspace=None, split: int = SPLIT_AUTO,
-                 check: bool = True) -> int:
+                 cta_pairs: int = PAIRS_AUTO, check: bool = True) -> int:
     """Fused attention + head->sequence all-to-all into `out_partitions` (P tensors [B,c_j,H,d]).
     trace: optional device int64 tensor of trace_numel(B, H, S) elements for per-tile stamps.
     part_heads: heads per partition row for a head-group launch (0 = H); the partitions are then
     given as device addresses already offset to the group's first head (see ulysses.py).
     workspace: optional zeroed uint8 tensor (alloc_workspace) that lets work items be split over
-    all CTAs by key blocks; split: which (SPLIT_AUTO, SPLIT_TAIL, SPLIT_ALL, SPLIT_NONE)."""
+    all CTAs by key blocks; split: which (SPLIT_AUTO, SPLIT_TAIL, SPLIT_ALL, SPLIT_NONE).
+    cta_pairs: PAIRS_ON runs the work on two-CTA clusters sharing each K/V block (M = 256 MMAs),
+    PAIRS_OFF one CTA per item, PAIRS_AUTO lets the library choose."""
     lib = load()
     shp = shape_of(q, k, v)
     parts = _ptr_array(out_partitions)
     _check_trace(trace, shp)
-    opts = _opts(store_kind, grid, timeout_ns, inject_stall, tile_order, trace, part_heads, workspace, split)
+    opts = _opts(store_kind, grid, timeout_ns, inject_stall, tile_order, trace, part_heads, workspace, split,
+                 cta_pairs)
     rc = lib.attn_a2a_fwd_ex(_ptr(q), _ptr(k), _ptr(v), ctypes.byref(shp), int(P), float(scale), parts,
                              _ptr(dev_status), ctypes.byref(opts), _stream(stream))
     return _check(rc, "attn_a2a_fwd", check)
@@ -264,12 +269,12 @@ def attn_a2a_fwd(q, k, v, P: int, scale: float, out_partitions, dev_status=None,
 
 def attn_a2a_fwd_contig(q, k, v, scale: float, out, dev_status=None, stream=None, store_kind: int = 0,
                         grid: int = 0, timeout_ns: int = 0, trace=None, workspace=None, split: int = SPLIT_AUTO,
-                        check: bool = True) -> int:
+                        cta_pairs: int = PAIRS_AUTO, check: bool = True) -> int:
     """The same kernel with a contiguous [B, H, S, d] output ("attention alone")."""
     lib = load()
     shp = shape_of(q, k, v)
     _check_trace(trace, shp)
-    opts = _opts(store_kind, grid, timeout_ns, 0, 0, trace, 0, workspace, split)
+    opts = _opts(store_kind, grid, timeout_ns, 0, 0, trace, 0, workspace, split, cta_pairs)
     rc = lib.attn_a2a_fwd_contig_ex(_ptr(q), _ptr(k), _ptr(v), ctypes.byref(shp), float(scale), _ptr(out),
                                     _ptr(dev_status), ctypes.byref(opts), _stream(stream))
     return _check(rc, "attn_a2a_fwd_contig", check)

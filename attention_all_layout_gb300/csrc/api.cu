@@ -196,7 +196,7 @@ int fwd_common(const void* q, const void* k, const void* v, const attn_a2a_shape
                           opts->tile_order < 0 || opts->tile_order > 1 ||
                           (reinterpret_cast<uintptr_t>(opts->trace) & 7u) != 0 || opts->part_heads < 0 ||
                           (opts->part_heads > 0 && !a2a) || opts->split < ATTN_A2A_SPLIT_AUTO ||
-                          opts->split > ATTN_A2A_SPLIT_NONE))
+                          opts->split > ATTN_A2A_SPLIT_NONE || opts->cta_pairs < 0 || opts->cta_pairs > 2))
     return ATTN_A2A_EINVAL;
   // the bulk-store epilogue exists for the contiguous layout and for the
   // all-to-all layout with up to 8 partitions

@@ -304,6 +304,22 @@ int launch_fa_tc(const void* q, const void* k, const void* v, const attn_a2a_sha
   // chunk-interleaved order: only when every chunk holds the same whole number of pairs
   if (opts.tile_order == 1 && a2a && epi.P > 1 && epi.crem == 0 && epi.cbase % (2 * tc::kBM) == 0)
     p.interleave = epi.cbase / (2 * tc::kBM);
+  // CTA pairs (cta_group::2 MMAs over two SMs): d = 128, bulk-store
+  // epilogue, sequence order, untraced, and no split schedule
+  const bool pair_ok = shp.d == 128 && bulk && p.interleave <= 1 && opts.trace == nullptr;
+  if (opts.cta_pairs == 1 && !pair_ok) return ATTN_A2A_EUNSUPPORTED;
+  if (pair_ok && opts.cta_pairs == 1) {
+    // each CTA of a pair loads half of every key block: K in 64-row boxes
+    if (!make_map(&maps.k[0], k, shp.B, shp.H, shp.S, shp.d, shp.k_sb, shp.k_sh, shp.k_ss, 64))
+      return ATTN_A2A_ECUDA;
+    p.nquad = (p.npair + 1) / 2;
+    p.total = shp.B * shp.H * p.nquad;
+    p.tail_first = p.total;
+    p.tail_len = 0;
+    const int want = opts.grid > 0 ? opts.grid : num_sms_current_device();
+    if (want <= 0) return ATTN_A2A_ECUDA;
+    return launch_fa_tc_pair(maps, p, a2a ? tc::kModeA2AT : tc::kModeContigT, want, stream);
+  }
   const int grid = grid_for(p, opts);
   if (grid <= 0) return ATTN_A2A_ECUDA;
   bool whole = false;

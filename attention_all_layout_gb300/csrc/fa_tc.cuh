@@ -78,15 +78,22 @@ constexpr int kRegsLow = 80;
 constexpr int kRegsHigh = 208;
 static_assert(128 * kRegsLow + 256 * kRegsHigh <= kThreads * kLaunchRegs, "register split exceeds the launch budget");
 
-template <int D>
+// PAIR: the CTA-pair kernel (d = 128), whose K/V stages hold this CTA's
+// half of a block - keys 64 r .. 64 r + 63 of K (two 64-row atoms), columns
+// 64 r .. 64 r + 63 of V (one 128-row atom) for rank r - so twice as many
+// stages fit in the same shared memory.
+template <int D, bool PAIR = false>
 struct Cfg {
   static_assert(D == 64 || D == 128, "head dim");
-  static constexpr int NSTAGE = (D == 128) ? 4 : 6;
+  static_assert(!PAIR || D == 128, "CTA pairs split V by 64-column atoms: d = 128 only");
   static constexpr int TILE_BYTES = 128 * D * 2;  // one Q, K or V tile (128 rows x d bf16)
+  static constexpr int KV_BYTES = PAIR ? TILE_BYTES / 2 : TILE_BYTES;  // one K/V stage
+  static constexpr int NSTAGE = PAIR ? 8 : (D == 128) ? 4 : 6;
   static constexpr int ATOM_BYTES = 128 * 128;    // 128 rows x one 128-byte swizzle column
+  static constexpr int K_ATOM_BYTES = KV_BYTES / (D / 64);  // a K stage's 128-byte swizzle column
   static constexpr int Q_OFF = 0;
   static constexpr int KV_OFF = 2 * TILE_BYTES;
-  static constexpr int BAR_OFF = KV_OFF + NSTAGE * TILE_BYTES;
+  static constexpr int BAR_OFF = KV_OFF + NSTAGE * KV_BYTES;
   // barrier slots
   static constexpr int QF = 0, QE = 2, SF = 4, OF = 6, OE = 8, KVF = 10;
   static constexpr int KVE = KVF + NSTAGE;
@@ -176,7 +183,8 @@ struct Params {
   int B, H, S;
   int nblk;   // query tiles per head = key blocks per head (ceil(S/128), or the per-partition count)
   int npair;  // ceil(nblk / 2): work items per head
-  int total;  // B * H * npair
+  int total;  // B * H * npair, or B * H * nquad for the CTA-pair kernel
+  int nquad;  // CTA-pair kernel: ceil(npair / 2) units of two pairs per head, one pair per CTA
   float scale_log2;
   int* dev_status;
   unsigned long long timeout_ns;
@@ -331,9 +339,17 @@ __device__ __forceinline__ bool tail_piece(const Params& p, int k, Piece& out) {
 // roles keep no other loop state; false past the last piece. The plain kernel
 // (SPLIT = false) runs whole items blockIdx.x, blockIdx.x + grid, ... below
 // p.total; the tail kernel (SPLIT = true) runs only this CTA's tail pieces.
-template <bool SPLIT>
+// The CTA-pair kernel (PAIR = true) runs one unit per cluster at a time: both
+// CTAs of cluster c run units c, c + grid / 2, ...
+template <bool SPLIT, bool PAIR = false>
 __device__ __forceinline__ bool piece_at(const Params& p, int it, Piece& out) {
-  if constexpr (!SPLIT) {
+  if constexpr (PAIR) {
+    static_assert(!SPLIT, "the CTA-pair kernel has no split schedule");
+    const int n = static_cast<int>(gridDim.x) / 2;
+    const int item = static_cast<int>(blockIdx.x) / 2 + it * n;
+    out = Piece{item, 0, p.nblk, 0};
+    return item < p.total;
+  } else if constexpr (!SPLIT) {
     const int item = static_cast<int>(blockIdx.x) + it * static_cast<int>(gridDim.x);
     out = Piece{item, 0, p.nblk, 0};
     return item < p.total;
@@ -342,8 +358,19 @@ __device__ __forceinline__ bool piece_at(const Params& p, int it, Piece& out) {
   }
 }
 
+// For the CTA-pair kernel `item` is a unit (b, h, quad): rank r of the
+// cluster takes query-tile pair 2 quad + r (past the head's last pair when
+// npair is odd: rows beyond S, read as zeros and never stored).
+template <bool PAIR = false>
 __device__ __forceinline__ Item decode_item(const Params& p, int item) {
   Item it;
+  if constexpr (PAIR) {
+    it.pair = 2 * (item % p.nquad) + static_cast<int>(cluster_ctarank());
+    const int bh = item / p.nquad;
+    it.h = bh % p.H;
+    it.b = bh / p.H;
+    return it;
+  }
   it.pair = item % p.npair;
   if (p.interleave > 1) {
     // i-th item of a head -> pair (i mod P) * pairs_per_chunk + i / P: neighbouring
@@ -358,11 +385,19 @@ __device__ __forceinline__ Item decode_item(const Params& p, int item) {
 }
 
 // ------------------------------------------------------------------ producer
-template <int D, int MODE, int NMAP, bool SPLIT>
+// PAIR: each CTA loads its own Q tiles and its half of every K/V block into
+// its own shared memory; all of them complete on the leader's QF/KVF
+// barriers, on which only the leader announces the pair's bytes.
+template <int D, int MODE, int NMAP, bool SPLIT, bool PAIR = false>
 __device__ void producer_role(const Params& p, const Maps<NMAP>* maps, uint32_t sbase, uint32_t bar0,
                               const WaitCtl& w) {
-  using C = Cfg<D>;
+  using C = Cfg<D, PAIR>;
+  static_assert(!PAIR || (!kSegLoads<MODE> && MODE != kModeS2S), "CTA pairs load head-sharded inputs only");
   auto BAR = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const bool lead = rank == 0;
+  // the barrier a load completes on: the leader's for a pair
+  auto FBAR = [&](int i) { return PAIR ? mapa_shared(BAR(i), 0) : BAR(i); };
   const uint64_t pol_kv = l2_policy_evict_last();  // K/V are re-read by every query tile of the head
   const uint64_t pol_q = l2_policy_evict_first();  // each Q tile is read once
   uint32_t kv_it = 0;
@@ -388,18 +423,22 @@ __device__ void producer_role(const Params& p, const Maps<NMAP>* maps, uint32_t 
         tma_load_4d(piece + a * C::ATOM_BYTES, &tmaps[j], bar, a * 64, l, wi.h, wi.b, pol);
     }
   };
-  for (Piece pc; ok && piece_at<SPLIT>(p, it, pc); ++it) {
+  for (Piece pc; ok && piece_at<SPLIT, PAIR>(p, it, pc); ++it) {
     const int k0 = pc.k0, nb = pc.k1 - pc.k0;
-    const Item wi = decode_item(p, pc.item);
+    const Item wi = decode_item<PAIR>(p, pc.item);
     auto load_q = [&](int t) -> bool {
       if (!mbar_wait(BAR(C::QE + t), (it & 1) ^ 1, w)) return false;
-      mbar_arrive_expect_tx(BAR(C::QF + t), C::TILE_BYTES);
+      if (lead) mbar_arrive_expect_tx(BAR(C::QF + t), PAIR ? 2 * C::TILE_BYTES : C::TILE_BYTES);
       const uint32_t dst = sbase + C::Q_OFF + t * C::TILE_BYTES;
       int qt = 2 * wi.pair + t;  // past the last tile (odd count): rows past S read as zeros,
       if (MODE == kModeS2S && qt >= p.nblk) qt = p.nblk - 1;  // or a real tile whose rows are not stored
       const Blk bq = locate_block<MODE>(p, qt);
       if constexpr (kSegLoads<MODE>) {
         load_segments(dst, maps->q, BAR(C::QF + t), bq.row, wi, pol_q);
+      } else if constexpr (PAIR) {
+#pragma unroll
+        for (int a = 0; a < D / 64; ++a)
+          tma_load_4d_pair(dst + a * C::ATOM_BYTES, &maps->q[0], FBAR(C::QF + t), a * 64, bq.row, wi.h, wi.b, pol_q);
       } else {
 #pragma unroll
         for (int a = 0; a < D / 64; ++a)
@@ -417,10 +456,21 @@ __device__ void producer_role(const Params& p, const Maps<NMAP>* maps, uint32_t 
       const uint32_t s = kv_it % C::NSTAGE;
       const uint32_t ph = (kv_it / C::NSTAGE) & 1;
       if (!mbar_wait(BAR(C::KVE + s), ph ^ 1, w)) return false;
-      mbar_arrive_expect_tx(BAR(C::KVF + s), C::TILE_BYTES);
-      const uint32_t dst = sbase + C::KV_OFF + s * C::TILE_BYTES;
+      if (lead) mbar_arrive_expect_tx(BAR(C::KVF + s), C::TILE_BYTES);  // the pair's two halves make one tile
+      const uint32_t dst = sbase + C::KV_OFF + s * C::KV_BYTES;
       if constexpr (kSegLoads<MODE>) {
         load_segments(dst, is_v ? maps->v : maps->k, BAR(C::KVF + s), bk.row, wi, pol_kv);
+      } else if constexpr (PAIR) {
+        // K: keys 64 r .. 64 r + 63 (the map's box is 64 rows), both column
+        // atoms; V: all 128 keys of column atom r
+        if (is_v) {
+          tma_load_4d_pair(dst, m, FBAR(C::KVF + s), static_cast<int>(rank) * 64, bk.row, wi.h, wi.b, pol_kv);
+        } else {
+#pragma unroll
+          for (int a = 0; a < D / 64; ++a)
+            tma_load_4d_pair(dst + a * C::K_ATOM_BYTES, m, FBAR(C::KVF + s), a * 64,
+                             bk.row + static_cast<int>(rank) * 64, wi.h, wi.b, pol_kv);
+        }
       } else {
 #pragma unroll
         for (int a = 0; a < D / 64; ++a)
@@ -433,9 +483,11 @@ __device__ void producer_role(const Params& p, const Maps<NMAP>* maps, uint32_t 
     kw.next(p);
     for (int j = 1; ok && j < nb; ++j, kw.next(p)) ok = load_kv(false) && load_kv(true);
   }
-  if (!ok) {
+  if (!ok && lead) {
     // Aborting: wait (bounded) for the copies this thread started, so none
-    // lands in shared memory after the CTA has exited.
+    // lands in shared memory after the CTA has exited. (A pair's copies all
+    // complete on the leader's barriers, and neither CTA of a pair exits
+    // before the other has finished.)
     const uint32_t n = kv_it < static_cast<uint32_t>(C::NSTAGE) ? kv_it : C::NSTAGE;
     for (uint32_t i = 0; i < n; ++i) {
       const uint32_t idx = kv_it - 1 - i;
@@ -447,36 +499,48 @@ __device__ void producer_role(const Params& p, const Maps<NMAP>* maps, uint32_t 
 }
 
 // ------------------------------------------------------------------ MMA issuer
-template <int D, bool SPLIT>
+// PAIR: run by the leader alone; every MMA spans both CTAs (M = 256: 128 query
+// rows of each, K and V from both halves) and every commit arrives on the
+// barrier of both CTAs.
+template <int D, bool SPLIT, bool PAIR = false>
 __device__ void mma_role(const Params& p, uint32_t sbase, uint32_t bar0, uint32_t tmem,
                          const WaitCtl& w) {
-  using C = Cfg<D>;
+  using C = Cfg<D, PAIR>;
   auto BAR = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
-  constexpr uint32_t kIdescQK = idesc_bf16_f32(kBM, kBN, false, false);  // Q, K both K-major
-  constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, D, false, true);     // V is MN-major (d contiguous)
+  constexpr int kM = PAIR ? 2 * kBM : kBM;
+  constexpr uint32_t kIdescQK = idesc_bf16_f32(kM, kBN, false, false);  // Q, K both K-major
+  constexpr uint32_t kIdescPV = idesc_bf16_f32(kM, D, false, true);     // V is MN-major (d contiguous)
+  auto umma_commit = [](uint32_t bar) {
+    if constexpr (PAIR) umma_commit_pair(bar);
+    else ::attn_a2a::umma_commit(bar);
+  };
   uint32_t kv_it = 0;
   uint32_t ev_a = 0, ev_b = 0, ev_c = 0;  // events consumed per kind
   bool ok = true;
 
   auto issue_qk = [&](int t, uint32_t sK) {
     const uint32_t qa = sbase + C::Q_OFF + t * C::TILE_BYTES;
-    const uint32_t kb = sbase + C::KV_OFF + sK * C::TILE_BYTES;
+    const uint32_t kb = sbase + C::KV_OFF + sK * C::KV_BYTES;
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
       const uint32_t off = (kk / 4) * C::ATOM_BYTES + (kk % 4) * 32;
-      umma_ss(tmem + t * 128, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
-              kIdescQK, kk > 0 ? 1u : 0u);
+      const uint32_t offk = (kk / 4) * C::K_ATOM_BYTES + (kk % 4) * 32;
+      const uint64_t da = sdesc_sw128(qa + off, 16, 1024), db = sdesc_sw128(kb + offk, 16, 1024);
+      if constexpr (PAIR) umma_ss_pair(tmem + t * 128, da, db, kIdescQK, kk > 0 ? 1u : 0u);
+      else umma_ss(tmem + t * 128, da, db, kIdescQK, kk > 0 ? 1u : 0u);
     }
   };
   // O_t (+)= P_t V_j for key block j (counted from the piece's first) of a
   // piece of nb blocks; the relay has already seen P_t ready and O_t free.
   auto issue_pv = [&](int t, int j, uint32_t sV, int nb) {
-    const uint32_t vb = sbase + C::KV_OFF + sV * C::TILE_BYTES;
+    const uint32_t vb = sbase + C::KV_OFF + sV * C::KV_BYTES;
 #pragma unroll
     for (int kk = 0; kk < kBN / 16; ++kk) {
-      umma_ts(tmem + 256 + t * D, tmem + t * 128 + kk * 8,
-              sdesc_sw128(vb + kk * 2048, C::ATOM_BYTES, 1024), kIdescPV,
-              (j > 0 || kk > 0) ? 1u : 0u);
+      const uint64_t dv = sdesc_sw128(vb + kk * 2048, C::ATOM_BYTES, 1024);
+      if constexpr (PAIR)
+        umma_ts_pair(tmem + 256 + t * D, tmem + t * 128 + kk * 8, dv, kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+      else
+        umma_ts(tmem + 256 + t * D, tmem + t * 128 + kk * 8, dv, kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
     }
     if (t == 1) umma_commit(BAR(C::KVE + sV));  // V_j now read by both tiles
     if (j == nb - 1) umma_commit(BAR(C::OF + t));
@@ -490,7 +554,7 @@ __device__ void mma_role(const Params& p, uint32_t sbase, uint32_t bar0, uint32_
 
   for (int it = 0; ok; ++it) {
     Piece pc;
-    if (!piece_at<SPLIT>(p, it, pc)) break;
+    if (!piece_at<SPLIT, PAIR>(p, it, pc)) break;
     const int nb = pc.k1 - pc.k0;
     uint32_t sVprev = 0;
     if (!sync(C::EVA, ev_a)) { ok = false; break; }  // A: both Q tiles and the piece's first K
@@ -548,9 +612,11 @@ __device__ void mma_role(const Params& p, uint32_t sbase, uint32_t bar0, uint32_
 // completed, so its arrival cannot count toward the previous event; the
 // softmax threads' arrivals for an event need an S that is issued only after
 // the issuer consumed the previous one, so they cannot either.
-template <int D, bool SPLIT>
+// PAIR: run by the leader alone, on the leader's barriers, which count both
+// CTAs' loads and both CTAs' softmax and O-free arrivals.
+template <int D, bool SPLIT, bool PAIR = false>
 __device__ void relay_role(const Params& p, uint32_t bar0, const WaitCtl& w) {
-  using C = Cfg<D>;
+  using C = Cfg<D, PAIR>;
   auto BAR = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
   uint32_t kv_it = 0;
   uint32_t n_b = 0, n_c = 0;  // EVB / EVC events arrived for so far
@@ -567,7 +633,7 @@ __device__ void relay_role(const Params& p, uint32_t bar0, const WaitCtl& w) {
     ++n;
     return r;
   };
-  for (Piece pc; piece_at<SPLIT>(p, it, pc); ++it) {
+  for (Piece pc; piece_at<SPLIT, PAIR>(p, it, pc); ++it) {
     const int nb = pc.k1 - pc.k0;
     if (!(mbar_wait(BAR(C::QF + 0), it & 1, w) && mbar_wait(BAR(C::QF + 1), it & 1, w))) return;
     if (!kv_ready()) return;
@@ -719,16 +785,16 @@ __device__ __forceinline__ bool tile_store_target(const Params& p, const Item& w
 // (token STG, one phase per use). The owners of use u wait for that release of
 // use u - 1 before they arrive, so neither side gets more than one use ahead.
 // Before returning (also on an abort) it waits until its stores have completed.
-template <int D, int MODE, int NMAP, bool SPLIT>
+template <int D, int MODE, int NMAP, bool SPLIT, bool PAIR = false>
 __device__ void store_role(const Params& p, const Maps<NMAP>* maps, uint32_t stg, uint32_t bar0, const WaitCtl& w) {
-  using C = Cfg<D>;
+  using C = Cfg<D, PAIR>;
   auto BAR = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
   uint32_t n[2] = {0, 0};  // uses of each tile so far
   bool ok = true;
   for (int it = 0; ok; ++it) {
     Piece pc;
-    if (!piece_at<SPLIT>(p, it, pc)) break;
-    const Item wi = decode_item(p, pc.item);
+    if (!piece_at<SPLIT, PAIR>(p, it, pc)) break;
+    const Item wi = decode_item<PAIR>(p, pc.item);
     for (int t = 0; t < 2; ++t) {
       if (!mbar_wait(BAR(C::STGW + t), n[t]++ & 1u, w)) {
         ok = false;
@@ -862,12 +928,26 @@ __device__ __forceinline__ void line_store_rows(uint32_t wbuf, int lane, uint16_
   }
 }
 
-template <int D, int MODE, int NMAP, bool TRACE, bool SPLIT>
+template <int D, int MODE, int NMAP, bool TRACE, bool SPLIT, bool PAIR = false>
 __device__ void softmax_role(const Params& p, int t, uint32_t bar0, uint32_t tmem, const Maps<NMAP>* maps,
                              uint32_t stg, const WaitCtl& w) {
-  using C = Cfg<D>;
+  using C = Cfg<D, PAIR>;
   auto BAR = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  // This thread's arrival on an event of the MMA issuer (EVB, EVC, OE): a
+  // pair's events are the leader's barriers, on which the other CTA arrives
+  // once per warp for its 32 threads (warp-uniform call).
+  auto arrive_event = [&](int i) {
+    if constexpr (PAIR) {
+      if (rank != 0) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(mapa_shared(BAR(i), 0), 32);
+        return;
+      }
+    }
+    mbar_arrive(BAR(i));
+  };
   const int r = (warp & 3) * 32 + lane;  // this thread's row of the tile = its TMEM lane
   const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
   const uint32_t tS = tmem + lane_off + t * 128;
@@ -878,11 +958,11 @@ __device__ void softmax_role(const Params& p, int t, uint32_t bar0, uint32_t tme
     int item, nb;
     {
       Piece pc;
-      if (!piece_at<SPLIT>(p, it, pc)) break;
+      if (!piece_at<SPLIT, PAIR>(p, it, pc)) break;
       item = pc.item;
       nb = pc.k1 - pc.k0;
     }
-    const Item wi = decode_item(p, item);
+    const Item wi = decode_item<PAIR>(p, item);
     const int srow = (2 * wi.pair + t) * kBM + r;
     uint64_t tr_q0 = 0, tr_q1 = 0, tr_e0 = 0;  // trace stamps (TRACE only)
     long long tr_c0 = 0;
@@ -909,7 +989,7 @@ __device__ void softmax_role(const Params& p, int t, uint32_t bar0, uint32_t tme
     kb.reset(p);
     if constexpr (MODE != kModeS2S) {
       Piece pc;
-      piece_at<SPLIT>(p, it, pc);
+      piece_at<SPLIT, PAIR>(p, it, pc);
       kb.b = pc.k0;  // (the split tail is not used with per-partition blocks)
     }
     for (int j = 0; j < nb; ++j) {  // the piece's key blocks, counted from its first
@@ -967,7 +1047,7 @@ __device__ void softmax_role(const Params& p, int t, uint32_t bar0, uint32_t tme
       tc_fence_before();
       // P_t written: this thread's arrival on the issuer's event (B_j for tile 0,
       // C_{j+1} or E for tile 1)
-      if (!(p.inject_stall && t == 0 && j == 0 && it == 0)) mbar_arrive(BAR(t == 0 ? C::EVB : C::EVC));  // test hook
+      if (!(p.inject_stall && t == 0 && j == 0 && it == 0)) arrive_event(t == 0 ? C::EVB : C::EVC);  // test hook
     }
     // ---- epilogue: the tile owner stores its rows to their destination and moves on
     const bool got = __all_sync(0xffffffffu, mbar_wait(BAR(C::OF + t), it & 1, w));
@@ -999,7 +1079,7 @@ __device__ void softmax_role(const Params& p, int t, uint32_t bar0, uint32_t tme
     if constexpr (D == 128) tmem_ld_x128(tO, o);
     else tmem_ld_x64(tO, o);
     tc_fence_before();
-    mbar_arrive(BAR(C::OE + t));  // O_t may now be overwritten by the next item
+    arrive_event(C::OE + t);  // O_t may now be overwritten by the next item
     if constexpr (TRACE) {
       tr_e0 = globaltimer_ns();
       tr_c0 = clock64();
@@ -1074,10 +1154,13 @@ __device__ void softmax_role(const Params& p, int t, uint32_t bar0, uint32_t tme
 }
 
 // ------------------------------------------------------------------ kernel
-template <int D, int MODE, int NMAP, bool TRACE = false, bool SPLIT = false>
+// PAIR: launched in clusters of two CTAs (the CTA-pair kernel); the leader's
+// warps 1 and 2 run the pair's MMA issuer and relay, the other CTA's stay idle.
+template <int D, int MODE, int NMAP, bool TRACE = false, bool SPLIT = false, bool PAIR = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_tc_kernel(const __grid_constant__ Maps<NMAP> maps, const __grid_constant__ Params p) {
-  using C = Cfg<D>;
+  static_assert(!PAIR || (!TRACE && !SPLIT && kBulkStores<MODE>), "CTA pairs: plain bulk-store kernels only");
+  using C = Cfg<D, PAIR>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -1094,7 +1177,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(BAR(C::QE + t), 1);
       mbar_init(BAR(C::SF + t), 1);
       mbar_init(BAR(C::OF + t), 1);
-      mbar_init(BAR(C::OE + t), kBM);
+      mbar_init(BAR(C::OE + t), PAIR ? 2 * kBM : kBM);  // a pair's: both CTAs' rows
     }
     for (int s = 0; s < C::NSTAGE; ++s) {
       mbar_init(BAR(C::KVF + s), 1);
@@ -1105,8 +1188,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(BAR(C::STGW + 0), 4);  // one arrive per warp of the tile
     mbar_init(BAR(C::STGW + 1), 4);
     mbar_init(BAR(C::EVA), 1);
-    mbar_init(BAR(C::EVB), kBM + 1);
-    mbar_init(BAR(C::EVC), kBM + 1);
+    mbar_init(BAR(C::EVB), (PAIR ? 2 * kBM : kBM) + 1);
+    mbar_init(BAR(C::EVC), (PAIR ? 2 * kBM : kBM) + 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -1123,11 +1206,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  // a pair: neither CTA signals the other's barriers before they are
+  // initialised, and the leader issues no MMA before both TMEMs are allocated
+  if constexpr (PAIR) cluster_sync();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   // a tail kernel queued behind this one may launch now: it takes each SM
@@ -1137,26 +1228,31 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
+    const bool lead = !PAIR || cluster_ctarank() == 0;
     if (warp == 0) {
-      if (lane == 0) producer_role<D, MODE, NMAP, SPLIT>(p, &maps, sbase, bar0, w);
+      if (lane == 0) producer_role<D, MODE, NMAP, SPLIT, PAIR>(p, &maps, sbase, bar0, w);
     } else if (warp == 1) {
-      if (lane == 0) mma_role<D, SPLIT>(p, sbase, bar0, tmem, w);
+      if (lane == 0 && lead) mma_role<D, SPLIT, PAIR>(p, sbase, bar0, tmem, w);
     } else if (warp == 2) {
-      if (lane == 0) relay_role<D, SPLIT>(p, bar0, w);
+      if (lane == 0 && lead) relay_role<D, SPLIT, PAIR>(p, bar0, w);
     } else if constexpr (kBulkStores<MODE>) {
       // every bulk store has completed before the store role returns
-      if (lane == 0) store_role<D, MODE, NMAP, SPLIT>(p, &maps, sbase + C::STG_OFF, bar0, w);
+      if (lane == 0) store_role<D, MODE, NMAP, SPLIT, PAIR>(p, &maps, sbase + C::STG_OFF, bar0, w);
     }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
-    softmax_role<D, MODE, NMAP, TRACE, SPLIT>(p, (warp - 4) / 4, bar0, tmem, &maps, sbase + C::STG_OFF, w);
+    softmax_role<D, MODE, NMAP, TRACE, SPLIT, PAIR>(p, (warp - 4) / 4, bar0, tmem, &maps, sbase + C::STG_OFF, w);
   }
   tc_fence_before();
   __syncthreads();
+  // a pair: the leader's MMAs read the other CTA's shared memory and TMEM,
+  // and the other CTA arrives on the leader's barriers, up to the end
+  if constexpr (PAIR) cluster_sync();
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    if constexpr (PAIR) tmem_dealloc_pair(tmem, kTmemCols);
+    else tmem_dealloc(tmem, kTmemCols);
   }
 }
 

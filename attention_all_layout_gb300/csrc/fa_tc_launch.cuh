@@ -9,10 +9,15 @@
 
 namespace attn_a2a {
 
-template <int D, int MODE, int NMAP, bool TRACE = false, bool SPLIT = false>
+// PAIR: the CTA-pair kernel, launched in clusters of two; `grid` is then the
+// CTAs wanted, cut to an even count of at most twice the clusters that can be
+// resident at once (every cluster's CTAs wait on each other) and twice the
+// work units.
+template <int D, int MODE, int NMAP, bool TRACE = false, bool SPLIT = false, bool PAIR = false>
 int launch_t(const tc::Maps<NMAP>& maps, const tc::Params& p, int grid, cudaStream_t stream, bool pdl = false) {
-  auto kern = tc::fa_fwd_tc_kernel<D, MODE, NMAP, TRACE, SPLIT>;
-  constexpr int smem = tc::kStagedStores<MODE> ? tc::Cfg<D>::SMEM_ALLOC_STG : tc::Cfg<D>::SMEM_ALLOC;
+  auto kern = tc::fa_fwd_tc_kernel<D, MODE, NMAP, TRACE, SPLIT, PAIR>;
+  using C = tc::Cfg<D, PAIR>;
+  constexpr int smem = tc::kStagedStores<MODE> ? C::SMEM_ALLOC_STG : C::SMEM_ALLOC;
   // The in-kernel register split assumes exactly this launch register count;
   // with fewer registers at launch the softmax warpgroups could never obtain
   // their share, so refuse to launch rather than risk a stuck kernel.
@@ -21,6 +26,35 @@ int launch_t(const tc::Maps<NMAP>& maps, const tc::Params& p, int grid, cudaStre
   if (attr.numRegs != tc::kLaunchRegs) return ATTN_A2A_EUNSUPPORTED;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return ATTN_A2A_ECUDA;
+  if constexpr (PAIR) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(tc::kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute cl[1];
+    cl[0].id = cudaLaunchAttributeClusterDimension;
+    cl[0].val.clusterDim.x = 2;
+    cl[0].val.clusterDim.y = 1;
+    cl[0].val.clusterDim.z = 1;
+    cfg.attrs = cl;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3(2 * (grid / 2 > 0 ? grid / 2 : 1));
+    int resident = 0;
+    if (cudaOccupancyMaxActiveClusters(&resident, kern, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      return ATTN_A2A_ECUDA;
+    }
+    int clusters = grid / 2;
+    if (clusters > resident) clusters = resident;
+    if (clusters > p.total) clusters = p.total;
+    if (clusters < 1) return ATTN_A2A_EUNSUPPORTED;
+    cfg.gridDim = dim3(2 * clusters);
+    if (cudaLaunchKernelEx(&cfg, kern, maps, p) != cudaSuccess) {
+      cudaGetLastError();
+      return ATTN_A2A_ECUDA;
+    }
+    return ATTN_A2A_OK;
+  }
   if (pdl) {
     // the tail kernel, queued behind the plain one: launched with programmatic
     // stream serialisation, so its CTAs start as the plain kernel's CTAs exit
@@ -55,5 +89,10 @@ int launch_fa_tc_traced(const tc::Maps<1>& maps, const tc::Params& p, int d, int
 // schedule on its own.
 int launch_fa_tc_split(const tc::Maps<1>& maps, const tc::Params& p, int d, int mode, int grid,
                        cudaStream_t stream, bool pdl);
+
+// The CTA-pair instantiation (d = 128) of the two bulk-store modes,
+// kModeA2AT and kModeContigT; p counts work units (p.nquad per head) and
+// maps.k has 64-row boxes.
+int launch_fa_tc_pair(const tc::Maps<1>& maps, const tc::Params& p, int mode, int grid, cudaStream_t stream);
 
 }  // namespace attn_a2a

@@ -304,7 +304,11 @@ def main():
     ap.add_argument("--no-presets", action="store_true", help="skip timing the image, joint and long presets")
     ap.add_argument("--no-split", action="store_true",
                     help="no split-tail workspace: a partial last wave of work items leaves CTAs idle")
+    ap.add_argument("--cta-pairs", action="store_true",
+                    help="with --fused-only: run the fused call on CTA pairs (cta_group::2 MMAs), no split")
     args = ap.parse_args()
+    if args.cta_pairs and not args.fused_only:
+        ap.error("--cta-pairs times the fused call alone: give --fused-only too")
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
@@ -334,10 +338,12 @@ def main():
     o = torch.empty((cfg.B, cfg.H, cfg.S, cfg.d), dtype=torch.bfloat16, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     # split-tail workspace (a partial last wave of work items is divided over all CTAs)
-    ws = None if args.no_split else bd.alloc_workspace(cfg.d)
+    ws = None if args.no_split or args.cta_pairs else bd.alloc_workspace(cfg.d)
+    pairs = bd.PAIRS_ON if args.cta_pairs else bd.PAIRS_AUTO
 
     def fused():
-        bd.attn_a2a_fwd(q, k, v, cfg.P, cfg.scale, parts, dev_status=status, stream=stream, workspace=ws)
+        bd.attn_a2a_fwd(q, k, v, cfg.P, cfg.scale, parts, dev_status=status, stream=stream, workspace=ws,
+                        cta_pairs=pairs)
 
     def contig():
         bd.attn_a2a_fwd_contig(q, k, v, cfg.scale, o, dev_status=status, stream=stream, workspace=ws)
@@ -381,7 +387,8 @@ def main():
                               "unit": "TFLOP/s", "ms_per_step": ms, "steps": args.steps,
                               "config": {"workload": cfg.name, "B": cfg.B, "H": cfg.H, "S": cfg.S,
                                          "d": cfg.d, "P": cfg.P,
-                                         "split": device_split_plan(cfg) if ws is not None else None},
+                                         "split": device_split_plan(cfg) if ws is not None else None,
+                                         "cta_pairs": bool(args.cta_pairs)},
                               "clocks": clocks, "fused_only": True}),
                   flush=True)
         return 0

@@ -183,6 +183,21 @@ typedef struct {
                            in pieces); all other items are the same bytes.
                            attn_a2a_fwd_ex and attn_a2a_fwd_contig_ex only */
   long long workspace_bytes; /* size of workspace */
+  int cta_pairs;        /* 0 in normal use: the library chooses. 1 = run the work on CTA
+                           pairs: clusters of two CTAs on two SMs whose tensor cores
+                           compute each pair of query tiles' scores and outputs as one
+                           256-row MMA (tcgen05 cta_group::2), each CTA holding its own
+                           query tiles and half of every K and V block, so that each SM
+                           reads half the K/V bytes per key block from shared memory; a
+                           work unit is then four 128-row query tiles of one (b, h).
+                           Needs d = 128 and the bulk-store epilogue (store kind 1, or
+                           the automatic kind into device memory), tile_order = 0 and no
+                           trace; otherwise ATTN_A2A_EUNSUPPORTED. No split schedule:
+                           the workspace is not used. grid then counts CTAs of pairs (an
+                           odd count is cut to the even one below it). 2 = one CTA per
+                           work item, as without this option. Results are the same bytes
+                           as 2 (each row sums the same products in the same order).
+                           Other values: ATTN_A2A_EINVAL */
 } attn_a2a_opts;
 
 /* attn_a2a_opts.split */

@@ -94,6 +94,8 @@ def test_bad_options_rejected(lib):
     assert call_fwd(lib, opts=bd._opts(grid=-1)) == bd.EINVAL
     assert call_fwd(lib, opts=bd._opts(timeout_ns=-5)) == bd.EINVAL
     assert call_fwd(lib, opts=bd._opts(tile_order=2)) == bd.EINVAL
+    assert call_fwd(lib, opts=bd._opts(cta_pairs=3)) == bd.EINVAL
+    assert call_fwd(lib, opts=bd._opts(cta_pairs=-1)) == bd.EINVAL
 
 
 def test_store_kind_query(lib):

@@ -784,7 +784,9 @@ __device__ __forceinline__ bool tile_store_target(const Params& p, const Item& w
 // have read the staging buffer, and then releases the buffer to use u + 1
 // (token STG, one phase per use). The owners of use u wait for that release of
 // use u - 1 before they arrive, so neither side gets more than one use ahead.
-// Before returning (also on an abort) it waits until its stores have completed.
+// Before returning (also on an abort) it waits until its stores have read the
+// staging buffer: shared memory must outlive those reads, while the writes
+// themselves are complete, like any of the grid's, when the grid is.
 template <int D, int MODE, int NMAP, bool SPLIT, bool PAIR = false>
 __device__ void store_role(const Params& p, const Maps<NMAP>* maps, uint32_t stg, uint32_t bar0, const WaitCtl& w) {
   using C = Cfg<D, PAIR>;
@@ -810,7 +812,7 @@ __device__ void store_role(const Params& p, const Maps<NMAP>* maps, uint32_t stg
       mbar_arrive(BAR(C::STG));
     }
   }
-  bulk_wait_all();
+  bulk_wait_read_all();
 }
 
 // Partial piece of a split item: this thread's row of the tile - unnormalised
@@ -1236,7 +1238,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 2) {
       if (lane == 0 && lead) relay_role<D, SPLIT, PAIR>(p, bar0, w);
     } else if constexpr (kBulkStores<MODE>) {
-      // every bulk store has completed before the store role returns
+      // every bulk store has read the staging buffer before the store role returns
       if (lane == 0) store_role<D, MODE, NMAP, SPLIT, PAIR>(p, &maps, sbase + C::STG_OFF, bar0, w);
     }
   } else {

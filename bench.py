@@ -17,7 +17,8 @@ Prints one JSON line. Legs:
   attention-alone, serial (attention, then a separate permute) and whole-layer
                times, taken in turns with the fused call over three rounds
   other_presets_fused  the fused call on the image, joint and long presets
-               (CUDA events; context, not the headline)
+               (CUDA events; context, not the headline): image and joint
+               before the headline, long after every other leg
 `--impl reference` times the oracle arm instead (CPU, rank 0 only).
 Multi-GPU (torchrun): every rank runs an independent replica of the workload
 (no data-path collective); value is the sum over ranks / slowest rank's time.
@@ -362,6 +363,29 @@ def main():
     sampler = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
     sampler.start()
     time.sleep(0.3)
+    # ---- the other presets' fused call (context beside the headline; not the
+    # metric). The short ones (image, joint: milliseconds of work) first, so
+    # that they are not timed at the clock the long legs leave behind
+    presets = {}
+
+    def time_preset(name, when):
+        pc = workloads.CONFIGS[name]
+        pq, pk, pv = workloads.make_qkv(pc, seed=rank, device="cuda")
+        pparts = bd.alloc_partitions(pc.B, pc.S, pc.H, pc.d, pc.P)
+        pws = None if args.no_split else bd.alloc_workspace(pc.d)
+        n = 50 if pc.flops < 1e12 else 5
+        # median of three windows
+        pms = statistics.median(
+            time_events(lambda: bd.attn_a2a_fwd(pq, pk, pv, pc.P, pc.scale, pparts, dev_status=status,
+                                                stream=stream, workspace=pws), n, 3, stream) for _ in range(3))
+        presets[name] = {"ms": pms, "tflops": pc.flops / (pms * 1e-3) / 1e12, "steps": n, "timed": when,
+                         "shape": {"B": pc.B, "H": pc.H, "S": pc.S, "d": pc.d, "P": pc.P}}
+        del pq, pk, pv, pparts, pws
+        torch.cuda.empty_cache()
+
+    if cfg.name == "video" and not args.no_presets and not args.fused_only:
+        for name in ("image", "joint"):
+            time_preset(name, "before the headline")
     # ---- headline: the fused call, inputs resident in HBM
     for _ in range(args.warmup):
         fused()
@@ -470,24 +494,9 @@ def main():
                  "serial": "attention alone, permute, copy of the partitions to pinned host memory"}
     del hq, hk, hv, dq, dk, dv, dparts, hparts
 
-    # ---- the other presets' fused call (context beside the headline; not the metric)
-    presets = {}
+    # ---- the long preset, last: seconds of full load that would heat the headline
     if cfg.name == "video" and not args.no_presets:
-        for name in ("image", "joint", "long"):
-            pc = workloads.CONFIGS[name]
-            pq, pk, pv = workloads.make_qkv(pc, seed=rank, device="cuda")
-            pparts = bd.alloc_partitions(pc.B, pc.S, pc.H, pc.d, pc.P)
-            pws = None if args.no_split else bd.alloc_workspace(pc.d)
-            n = 50 if pc.flops < 1e12 else 5
-            # median of three windows: a short call timed right after the long legs
-            # otherwise catches the clock still settling
-            pms = statistics.median(
-                time_events(lambda: bd.attn_a2a_fwd(pq, pk, pv, pc.P, pc.scale, pparts, dev_status=status,
-                                                    stream=stream, workspace=pws), n, 3, stream) for _ in range(3))
-            presets[name] = {"ms": pms, "tflops": pc.flops / (pms * 1e-3) / 1e12, "steps": n,
-                             "shape": {"B": pc.B, "H": pc.H, "S": pc.S, "d": pc.d, "P": pc.P}}
-            del pq, pk, pv, pparts, pws
-            torch.cuda.empty_cache()
+        time_preset("long", "after the other legs")
     sampler.stop()
 
     peaks, peak_src = load_peaks()

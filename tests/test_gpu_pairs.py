@@ -9,7 +9,7 @@ holding its own query tiles and half of every K and V block.
   of four clusters running many units each through the K/V ring.
 * Byte for byte the same output as one CTA per work item (cta_pairs = 2): each
   row's scores and outputs are the same products summed in the same order, in
-  the all-to-all and the contiguous layout, up to the image preset's size.
+  the all-to-all and the contiguous layout, up to the video preset's size.
 * Refusals where the pair kernel does not exist (row stores, d = 64, the
   chunk-interleaved order, a trace), and the bounded waits of both CTAs when
   the first probabilities are withheld: ATTN_A2A_ETIMEOUT, and the context
@@ -101,3 +101,14 @@ def test_pairs_bounded_wait_reports_timeout():
     assert int(status.item()) == bd.ETIMEOUT
     g = fused(q, k, v, cfg.P, cfg.scale, cta_pairs=bd.PAIRS_ON)
     assert g.guards_intact()
+
+
+def test_pairs_video_preset_same_bytes():
+    # the full video shape: 2560 units of 256 key blocks on 76 clusters, the K/V
+    # ring of eight half stages wrapping many times per unit
+    cfg = workloads.CONFIGS["video"]
+    q, k, v = workloads.make_qkv(cfg, seed=14, device="cuda")
+    g1 = fused(q, k, v, cfg.P, cfg.scale, cta_pairs=bd.PAIRS_ON)
+    g2 = fused(q, k, v, cfg.P, cfg.scale, cta_pairs=bd.PAIRS_OFF, split=bd.SPLIT_NONE)
+    assert g1.guards_intact()
+    assert same_bytes(g1.parts, g2.parts)

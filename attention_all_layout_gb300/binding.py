@@ -27,6 +27,7 @@ EXPORTED = (
     "attn_a2a_fwd_contig",
     "attn_a2a_fwd_contig_ex",
     "attn_a2a_fwd_s2s",
+    "attn_a2a_fwd_s2s_ex",
     "attn_a2a_permute",
     "attn_a2a_fwd_simt",
     "attn_a2a_fwd_host",
@@ -107,6 +108,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.attn_a2a_fwd_contig.argtypes = [vp, vp, vp, shp, ctypes.c_float, vp, vp, vp]
     lib.attn_a2a_fwd_contig_ex.argtypes = [vp, vp, vp, shp, ctypes.c_float, vp, vp, opt, vp]
     lib.attn_a2a_fwd_s2s.argtypes = [pp, pp, pp, shp, cint, ctypes.c_float, pp, vp, vp]
+    lib.attn_a2a_fwd_s2s_ex.argtypes = [pp, pp, pp, shp, cint, ctypes.c_float, pp, vp, ctypes.POINTER(Opts), vp]
     lib.attn_a2a_permute.argtypes = [vp, shp, cint, pp, vp]
     lib.attn_a2a_fwd_simt.argtypes = [vp, vp, vp, shp, cint, ctypes.c_float, pp, vp]
     lib.attn_a2a_fwd_host.argtypes = [vp, vp, vp, shp, cint, ctypes.c_float, vp, vp, vp, pp, pp, vp, vp]
@@ -281,8 +283,11 @@ def attn_a2a_fwd_contig(q, k, v, scale: float, out, dev_status=None, stream=None
 
 
 def attn_a2a_fwd_s2s(q_parts, k_parts, v_parts, P: int, scale: float, out_partitions, dev_status=None,
-                     stream=None, check: bool = True) -> int:
-    """Sequence-sharded q, k, v partitions [B, c_j, H, d] in, sequence-sharded output out."""
+                     stream=None, store_kind: int = 0, grid: int = 0, timeout_ns: int = 0, workspace=None,
+                     split: int = SPLIT_AUTO, check: bool = True) -> int:
+    """Sequence-sharded q, k, v partitions [B, c_j, H, d] in, sequence-sharded output out.
+    workspace / split: the split schedule, as for attn_a2a_fwd (where tiles are counted over
+    the whole sequence)."""
     lib = load()
     B, _, H, d = q_parts[0].shape
     S = sum(t.shape[1] for t in q_parts)
@@ -291,8 +296,10 @@ def attn_a2a_fwd_s2s(q_parts, k_parts, v_parts, P: int, scale: float, out_partit
             if t.dtype != torch.bfloat16 or (t.numel() and not t.is_contiguous()):
                 raise ValueError("partitions must be contiguous bf16 [B, c_j, H, d]")
     shp = plain_shape(B, H, S, d)
-    rc = lib.attn_a2a_fwd_s2s(_ptr_array(q_parts), _ptr_array(k_parts), _ptr_array(v_parts), ctypes.byref(shp),
-                              int(P), float(scale), _ptr_array(out_partitions), _ptr(dev_status), _stream(stream))
+    opts = _opts(store_kind, grid, timeout_ns, 0, 0, None, 0, workspace, split)
+    rc = lib.attn_a2a_fwd_s2s_ex(_ptr_array(q_parts), _ptr_array(k_parts), _ptr_array(v_parts), ctypes.byref(shp),
+                                 int(P), float(scale), _ptr_array(out_partitions), _ptr(dev_status),
+                                 ctypes.byref(opts), _stream(stream))
     return _check(rc, "attn_a2a_fwd_s2s", check)
 
 

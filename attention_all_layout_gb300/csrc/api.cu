@@ -328,8 +328,25 @@ int attn_a2a_fwd_contig(const void* q, const void* k, const void* v, const attn_
 int attn_a2a_fwd_s2s(const void* const* q_parts, const void* const* k_parts,
                      const void* const* v_parts, const attn_a2a_shape* shp, int P, float scale,
                      void* const* out_partitions, int* dev_status, void* stream) {
+  return attn_a2a_fwd_s2s_ex(q_parts, k_parts, v_parts, shp, P, scale, out_partitions, dev_status, nullptr, stream);
+}
+
+int attn_a2a_fwd_s2s_ex(const void* const* q_parts, const void* const* k_parts,
+                        const void* const* v_parts, const attn_a2a_shape* shp, int P, float scale,
+                        void* const* out_partitions, int* dev_status, const attn_a2a_opts* opts, void* stream) {
   if (shp == nullptr || q_parts == nullptr || k_parts == nullptr || v_parts == nullptr)
     return ATTN_A2A_EINVAL;
+  if (opts != nullptr && (opts->store_kind < 0 || opts->store_kind > 3 || opts->grid < 0 || opts->timeout_ns < 0 ||
+                          opts->inject_stall < 0 || opts->inject_stall > 1 || opts->tile_order < 0 ||
+                          opts->tile_order > 1 || (reinterpret_cast<uintptr_t>(opts->trace) & 7u) != 0 ||
+                          opts->part_heads < 0 || opts->split < ATTN_A2A_SPLIT_AUTO ||
+                          opts->split > ATTN_A2A_SPLIT_NONE || opts->cta_pairs < 0 || opts->cta_pairs > 2))
+    return ATTN_A2A_EINVAL;
+  // what the whole-layer kernels do not have: whole-line row stores, the
+  // chunk-interleaved order, a trace, head-group partitions, CTA pairs
+  if (opts != nullptr && (opts->store_kind == 3 || opts->tile_order != 0 || opts->trace != nullptr ||
+                          opts->part_heads != 0 || opts->cta_pairs == 1))
+    return ATTN_A2A_EUNSUPPORTED;
   if (shp->B < 0 || shp->H < 0 || shp->S < 0 || shp->d <= 0) return ATTN_A2A_EINVAL;
   if (!std::isfinite(scale) || scale < 0.f) return ATTN_A2A_EINVAL;
   if (shp->d != 64 && shp->d != 128) return ATTN_A2A_EUNSUPPORTED;
@@ -353,7 +370,22 @@ int attn_a2a_fwd_s2s(const void* const* q_parts, const void* const* k_parts,
     }
   }
   if (partitions_alias_inputs(*shp, epi, in, nin)) return ATTN_A2A_EINVAL;
-  const attn_a2a_opts o = default_opts();
+  if (opts != nullptr && opts->workspace != nullptr) {
+    // split scratch: aligned, and apart from every input and output partition
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(opts->workspace);
+    if ((lo & 255u) != 0 || opts->workspace_bytes <= 0) return ATTN_A2A_EINVAL;
+    const Span ws{lo, lo + static_cast<uintptr_t>(opts->workspace_bytes)};
+    for (int i = 0; i < nin; ++i)
+      if (overlaps(ws, in[i])) return ATTN_A2A_EINVAL;
+    for (int j = 0; j < epi.P; ++j) {
+      const int c = epi.cbase + (j < epi.crem ? 1 : 0);
+      if (c == 0) continue;
+      const uintptr_t plo = reinterpret_cast<uintptr_t>(epi.part[j]);
+      if (overlaps(ws, Span{plo, plo + static_cast<uintptr_t>(shp->B) * c * shp->H * shp->d * 2u}))
+        return ATTN_A2A_EINVAL;
+    }
+  }
+  const attn_a2a_opts o = opts ? *opts : default_opts();
   return launch_fa_tc_s2s(q_parts, k_parts, v_parts, *shp, scale, epi, dev_status, o,
                           static_cast<cudaStream_t>(stream));
 }

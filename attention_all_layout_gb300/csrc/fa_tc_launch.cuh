@@ -95,4 +95,10 @@ int launch_fa_tc_split(const tc::Maps<1>& maps, const tc::Params& p, int d, int 
 // maps.k has 64-row boxes.
 int launch_fa_tc_pair(const tc::Maps<1>& maps, const tc::Params& p, int mode, int grid, cudaStream_t stream);
 
+// The split instantiation of the whole layer's global-tile modes (kModeS2SG,
+// kModeS2SGT; sequence-sharded inputs loaded in segments), as
+// launch_fa_tc_split.
+int launch_fa_tc_split_s2s(const tc::Maps<tc::kMaxS2SRanks>& maps, const tc::Params& p, int d, int mode, int grid,
+                           cudaStream_t stream, bool pdl);
+
 }  // namespace attn_a2a

@@ -432,7 +432,7 @@ def main():
         sq, sk, sv = ([t[:, :, st:st + c].permute(0, 2, 1, 3).contiguous()
                        for st, c in zip(_starts(cfg.S, cfg.P), bd.chunk_sizes(cfg.S, cfg.P))] for t in (q, k, v))
         legs["s2s"] = lambda: bd.attn_a2a_fwd_s2s(sq, sk, sv, cfg.P, cfg.scale, parts, dev_status=status,
-                                                  stream=stream)
+                                                  stream=stream, workspace=ws)
     turns = {name: [] for name in legs}
     for _ in range(3):
         for name, fn in legs.items():

@@ -286,6 +286,25 @@ int attn_a2a_fwd_s2s(const void* const* q_parts, const void* const* k_parts,
                      void* const* out_partitions, int* dev_status, void* stream);
 
 /*
+ * attn_a2a_fwd_s2s_ex - attn_a2a_fwd_s2s with options (opts may be NULL: as
+ * attn_a2a_fwd_s2s). Taken: store_kind 0-2, grid, timeout_ns, inject_stall,
+ * workspace / workspace_bytes and split, meaning what they mean for
+ * attn_a2a_fwd_ex; the split schedule applies where tiles are counted over
+ * the whole sequence (equal partitions of a multiple of 64 rows), and with
+ * the same split the result is then the same bytes as attn_a2a_fwd_ex's. The
+ * automatic choice (ATTN_A2A_SPLIT_AUTO) takes only the whole-schedule split
+ * here (the last wave's split measured slower for the layer); an explicit
+ * ATTN_A2A_SPLIT_TAIL is honoured. ATTN_A2A_EUNSUPPORTED for store_kind 3, tile_order 1, a
+ * trace, part_heads or cta_pairs 1, which the whole-layer kernels do not
+ * have; out-of-range values are ATTN_A2A_EINVAL. The workspace must not
+ * overlap any input or output partition.
+ */
+int attn_a2a_fwd_s2s_ex(const void* const* q_parts, const void* const* k_parts,
+                        const void* const* v_parts, const attn_a2a_shape* shp, int P, float scale,
+                        void* const* out_partitions, int* dev_status, const attn_a2a_opts* opts,
+                        void* stream);
+
+/*
  * attn_a2a_permute - the serial all-to-all on its own: a pure copy of a
  * contiguous [B, H, S, d] bf16 device tensor o into the P partitions
  * (same layout and chunk rule as attn_a2a_fwd). shp supplies B, H, S, d; its

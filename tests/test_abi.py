@@ -98,6 +98,27 @@ def test_bad_options_rejected(lib):
     assert call_fwd(lib, opts=bd._opts(cta_pairs=-1)) == bd.EINVAL
 
 
+def test_s2s_ex_options(lib):
+    # the whole layer's entry point with options: what its kernels do not have
+    # is refused before anything runs; out-of-range values are invalid
+    shp = bd.plain_shape(1, 8, 4096, 128)
+    parts = [FAKE * (16 + j) for j in range(8)]
+    q, k, v = ([FAKE * (64 + 8 * i + j) for j in range(8)] for i in range(3))
+    arr = lambda xs: (ctypes.c_void_p * 8)(*xs)
+
+    def call(**kw):
+        o = bd._opts(**kw)
+        return lib.attn_a2a_fwd_s2s_ex(arr(q), arr(k), arr(v), ctypes.byref(shp), 8, 0.1, arr(parts), None,
+                                       ctypes.byref(o), None)
+    assert call(store_kind=3) == bd.EUNSUPPORTED
+    assert call(tile_order=1) == bd.EUNSUPPORTED
+    assert call(part_heads=16) == bd.EUNSUPPORTED
+    assert call(cta_pairs=1) == bd.EUNSUPPORTED
+    assert call(store_kind=4) == bd.EINVAL
+    assert call(split=4) == bd.EINVAL
+    assert call(grid=-1) == bd.EINVAL
+
+
 def test_store_kind_query(lib):
     # the automatic kind: bulk tensor stores for the contiguous layout, and for
     # the all-to-all layout with P <= 8, at every length

@@ -2,7 +2,9 @@
 folded in (sequence-sharded q, k, v partitions in, sequence-sharded output
 out) against the float64 oracle, guard bands intact, and bit-identical to
 attn_a2a_fwd when every chunk is a whole number of 128-row tiles, or when the
-chunks are equal multiples of 64 rows (each tile then loaded as two halves)."""
+chunks are equal multiples of 64 rows (each tile then loaded as two halves),
+also with the split schedule (attn_a2a_fwd_s2s_ex with a workspace), where
+both calls run the same pieces."""
 import numpy as np
 import pytest
 import torch
@@ -74,3 +76,41 @@ def test_s2s_bit_identical_to_fused_on_whole_or_half_tiles(name):
     torch.cuda.synchronize()
     for x, y in zip(a, b):
         assert torch.equal(x.view(torch.int16), y.view(torch.int16))
+
+
+# The split schedule in the whole layer (attn_a2a_fwd_s2s_ex with a workspace):
+# the same pieces, partials and merges as the fused call's with the same
+# workspace setting, so the same bytes; and against the oracle.
+SPLIT_CASES = [
+    ("image", None, bd.SPLIT_AUTO, 0),                                    # automatic: the whole schedule
+    ("tail_h8_s8192", dict(B=1, H=8, S=8192, d=128, P=8), bd.SPLIT_TAIL, 0),
+    ("all_h8_s8192", dict(B=1, H=8, S=8192, d=128, P=8), bd.SPLIT_ALL, 0),
+    ("all_halves_c576", dict(B=1, H=8, S=4608, d=128, P=8), bd.SPLIT_ALL, 0),   # 64-row halves, row stores
+    ("tail_d64_grid40", dict(B=2, H=4, S=2048, d=64, P=4), bd.SPLIT_TAIL, 40),
+]
+
+
+@pytest.mark.parametrize("case", SPLIT_CASES, ids=[c[0] for c in SPLIT_CASES])
+def test_s2s_split_schedule_same_bytes_as_fused(case):
+    name, shape, split, grid = case
+    cfg = workloads.CONFIGS[name] if shape is None else workloads.AttnConfig(name, **shape)
+    B, H, S, d, P = cfg.B, cfg.H, cfg.S, cfg.d, cfg.P
+    q, k, v = workloads.make_qkv(cfg, seed=21)
+    dq, dk, dv = q.cuda(), k.cuda(), v.cuda()
+    ws = bd.alloc_workspace(d, grid)
+    g = GuardedPartitions(B, S, H, d, P)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    bd.attn_a2a_fwd_s2s(seq_shard(q, P), seq_shard(k, P), seq_shard(v, P), P, cfg.scale, g.parts, dev_status=status,
+                        workspace=ws, split=split, grid=grid)
+    ref = GuardedPartitions(B, S, H, d, P)
+    bd.attn_a2a_fwd(dq, dk, dv, P, cfg.scale, ref.parts, dev_status=status, workspace=bd.alloc_workspace(d, grid),
+                    split=split, grid=grid)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert g.guards_intact()
+    for a, b in zip(g.parts, ref.parts):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    if B * H * S * S <= 8 * 4608 * 4608:  # the oracle where it takes seconds
+        want = orc.head_to_seq_partitions(orc.attention_fp64(q, k, v, cfg.scale), P)
+        for j, (got, w) in enumerate(zip(g.parts, want)):
+            compare(orc.as_f64(got), w, f"{name} partition {j}")

@@ -99,14 +99,14 @@ bool make_map(CUtensorMap* m, const void* base, int B, int H, int S, int d, long
 // (d, head, row, batch) with heads [0, H) of a row of H_row heads; box of 64
 // columns x 1 head x 128 rows, 128-byte swizzle (the staging buffer's
 // layout). Rows past c_j are not written by a store.
-bool make_out_map(CUtensorMap* m, void* base, int B, int H, int H_row, int c, int d) {
+bool make_out_map(CUtensorMap* m, void* base, int B, int H, int H_row, int c, int d, int box_rows = 128) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
   cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(c),
                         static_cast<cuuint64_t>(B)};
   cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(H_row) * d * 2,
                            static_cast<cuuint64_t>(c) * H_row * d * 2};
-  cuuint32_t box[4] = {64, 1, 128, 1};
+  cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(box_rows), 1};
   cuuint32_t estride[4] = {1, 1, 1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims, strides, box, estride,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -282,12 +282,18 @@ int launch_fa_tc(const void* q, const void* k, const void* v, const attn_a2a_sha
     }
   }
   const bool bulk = kind == 1;
+  // Equal partitions of an odd multiple of 64 rows (the joint preset's 576)
+  // cut every other partition boundary through a 128-row tile; every 64-row
+  // half of a tile then lies in one partition, so each tile goes out as two
+  // half-tile tensor stores instead of row stores for the cut tiles.
+  const bool halves = bulk && a2a && epi.P > 1 && epi.crem == 0 && epi.cbase % tc::kBM == tc::kBM / 2;
   if (bulk && a2a) {
     const int h_row = epi.hstride > 0 ? epi.hstride : shp.H;
     for (int j = 0; j < epi.P; ++j) {
       const int c = epi.cbase + (j < epi.crem ? 1 : 0);
       if (c == 0) continue;
-      if (!make_out_map(&maps.o[j], epi.part[j], shp.B, shp.H, h_row, c, shp.d)) return ATTN_A2A_ECUDA;
+      if (!make_out_map(&maps.o[j], epi.part[j], shp.B, shp.H, h_row, c, shp.d, halves ? tc::kBM / 2 : tc::kBM))
+        return ATTN_A2A_ECUDA;
     }
   }
   if (bulk && !a2a) {  // [B, H, S, d] contiguous, addressed like the inputs
@@ -304,6 +310,7 @@ int launch_fa_tc(const void* q, const void* k, const void* v, const attn_a2a_sha
   p.npair = (p.nblk + 1) / 2;
   p.total = shp.B * shp.H * p.npair;
   p.epi = epi;
+  p.half_stores = halves ? 1 : 0;
   // chunk-interleaved order: only when every chunk holds the same whole number of pairs
   if (opts.tile_order == 1 && a2a && epi.P > 1 && epi.crem == 0 && epi.cbase % (2 * tc::kBM) == 0)
     p.interleave = epi.cbase / (2 * tc::kBM);
@@ -375,14 +382,14 @@ int launch_fa_tc_s2s(const void* const* qp, const void* const* kp, const void* c
   std::memset(&maps, 0, sizeof(maps));
   // Equal partitions whose length is a multiple of 64 but not of 128 would end
   // every partition in a half-empty block: count tiles over the whole sequence
-  // and load each as two 64-row pieces, each inside one partition (kModeS2SG,
-  // row stores: bulk stores on top of the doubled TMA loads measured 1.6-1.9 %
-  // slower on the joint preset). Partitions of a multiple of 128 rows tile the
-  // same either way; they take the global tiles with one 128-row piece where
-  // the automatic store kind is bulk (kModeS2SGT: the image preset's layer
-  // measured 1.4 % faster than with row stores), else the per-partition tiles
-  // of kModeS2S (measured 1-2 % faster than kModeS2SG at S = 32768). Other
-  // partition lengths count tiles per partition (kModeS2S).
+  // and load each as two 64-row pieces, each inside one partition, and store
+  // each tile as two 64-row halves (kModeS2SGT with half_stores: the joint
+  // preset's layer 0.1773-0.1818 ms against 0.1836-0.1891 with row stores,
+  // kModeS2SG). Partitions of a multiple of 128 rows tile the same either way;
+  // they take the global tiles with one 128-row piece where the automatic
+  // store kind is bulk (kModeS2SGT: the image preset's layer measured 1.4 %
+  // faster than with row stores), else the per-partition tiles of kModeS2S.
+  // Other partition lengths count tiles per partition (kModeS2S).
   int auto_kind = resolve_store_kind(shp.S, epi.P, true, opts.store_kind, kBulkS2SMaxBlocks);
   if (auto_kind == 0) return ATTN_A2A_EUNSUPPORTED;
   if (auto_kind == 1) {  // bulk stores only into this device's memory (see launch_fa_tc)
@@ -396,7 +403,9 @@ int launch_fa_tc_s2s(const void* const* qp, const void* const* kp, const void* c
   const bool equal64 = epi.crem == 0 && epi.cbase > 0 && epi.cbase % (tc::kBM / 2) == 0;
   const int seg = epi.cbase % tc::kBM == 0 ? tc::kBM : tc::kBM / 2;
   const bool global_tiles = equal64 && (seg < tc::kBM || auto_kind == 1);
-  const int kind = seg < tc::kBM && opts.store_kind == 0 ? 2 : auto_kind;
+  const int kind = auto_kind;
+  // partitions of an odd multiple of 64 rows: tiles stored in two 64-row halves
+  const bool halves = kind == 1 && global_tiles && seg < tc::kBM;
   const long long row = static_cast<long long>(shp.H) * shp.d;  // partition j is [B, c_j, H, d]
   for (int j = 0; j < epi.P; ++j) {
     const int c = epi.cbase + (j < epi.crem ? 1 : 0);
@@ -412,6 +421,7 @@ int launch_fa_tc_s2s(const void* const* qp, const void* const* kp, const void* c
   common_params(p, shp, scale, dev_status, opts);
   if (global_tiles) {
     p.seg = seg;
+    p.half_stores = halves ? 1 : 0;
     p.nblk = (shp.S + tc::kBM - 1) / tc::kBM;
     p.npair = (p.nblk + 1) / 2;
     p.total = shp.B * shp.H * p.npair;
@@ -431,7 +441,9 @@ int launch_fa_tc_s2s(const void* const* qp, const void* const* kp, const void* c
     }
     if (kind == 1) {
       for (int j = 0; j < epi.P; ++j)
-        if (!make_out_map(&maps.o[j], epi.part[j], shp.B, shp.H, shp.H, epi.cbase, shp.d)) return ATTN_A2A_ECUDA;
+        if (!make_out_map(&maps.o[j], epi.part[j], shp.B, shp.H, shp.H, epi.cbase, shp.d,
+                          halves ? tc::kBM / 2 : tc::kBM))
+          return ATTN_A2A_ECUDA;
     }
     const int mode = kind == 1 ? tc::kModeS2SGT : tc::kModeS2SG;
     auto plain = [&](const tc::Params& pp) -> int {

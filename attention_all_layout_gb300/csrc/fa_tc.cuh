@@ -192,6 +192,8 @@ struct Params {
   int nb_big, nb_small;  // kModeS2S: 128-row blocks of a longer / shorter chunk
   int interleave;        // > 1: chunk-interleaved item order with this many pairs per chunk
   int seg;               // kModeS2SG(T): rows per TMA box of the sequence-sharded loads (128 or 64)
+  int half_stores;       // kModeA2AT, kModeS2SGT: every tile stored as two 64-row halves, each into the partition
+                         // holding it (equal partitions of an odd multiple of 64 rows; 64-row output boxes)
   long long* trace;      // traced instantiations only: kTraceRecord int64 per (item, tile, warp)
   // Split schedule (see tail_piece): the key blocks of items [tail_first,
   // total) are divided over the CTAs, tail_len blocks per CTA; tail_first =
@@ -766,10 +768,11 @@ __device__ __forceinline__ bool tile_store_target(const Params& p, const Item& w
   } else {
     int j0, l0, c0, j1, l1, c1;
     chunk_of_row(p.epi, s0, j0, l0, c0);
-    chunk_of_row(p.epi, min(s0 + kBM, p.S) - 1, j1, l1, c1);
     map = j0;
     y = wi.h;
     z = l0;
+    if (p.half_stores) return true;  // two halves, each inside one partition (store_role)
+    chunk_of_row(p.epi, min(s0 + kBM, p.S) - 1, j1, l1, c1);
     return j0 == j1 && j0 < kMaxStoreMaps;  // the whole tile lands in one partition
   }
 }
@@ -804,8 +807,25 @@ __device__ void store_role(const Params& p, const Maps<NMAP>* maps, uint32_t stg
       }
       int map, y, z;
       if (!(SPLIT && pc.kind == 1) && tile_store_target<MODE>(p, wi, t, map, y, z)) {
+        if (MODE != kModeContigT && p.half_stores) {
+          // rows [s, s + 64) of each half into the partition that holds them
+          // (a half starting at or past S has no rows)
+          const int s0 = (2 * wi.pair + t) * kBM;
 #pragma unroll
-        for (int a = 0; a < D / 64; ++a) tma_store_4d(&maps->o[map], stg + a * 128 * 128, a * 64, y, z, wi.b);
+          for (int h = 0; h < 2; ++h) {
+            const int s = s0 + h * (kBM / 2);
+            if (s < p.S) {
+              int j, l, c;
+              chunk_of_row(p.epi, s, j, l, c);
+#pragma unroll
+              for (int a = 0; a < D / 64; ++a)
+                tma_store_4d(&maps->o[j], stg + a * 128 * 128 + h * 64 * 128, a * 64, y, l, wi.b);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int a = 0; a < D / 64; ++a) tma_store_4d(&maps->o[map], stg + a * 128 * 128, a * 64, y, z, wi.b);
+        }
         bulk_commit_group();
         bulk_wait_read_all();  // the buffer may be reused once the stores have read it
       }

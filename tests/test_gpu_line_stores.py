@@ -8,6 +8,9 @@ and of the fused call storing into partitions in host memory.
   - the two kinds compute the same values and only write them differently -
   also for a head-group call into full-width partitions, with the split
   schedule, and in the traced instantiation.
+* Bulk tensor stores in two 64-row halves where equal partitions of an odd
+  multiple of 64 rows cut tiles in half: against the oracle and byte for byte
+  the row stores.
 * Into pinned host memory (the device stores straight into the host's
   partitions over the host link): the same bytes as into device memory, for
   kinds 2 and 3, at a small shape and at the image preset's size.
@@ -120,3 +123,26 @@ def test_bulk_stores_refused_outside_device_memory():
     bd.attn_a2a_fwd_contig(q, k, v, cfg.scale, o)
     torch.cuda.synchronize()
     assert torch.equal(o.view(torch.int16), dev.cpu().view(torch.int16))
+
+
+# Equal partitions of an odd multiple of 64 rows: every other partition
+# boundary cuts a 128-row tile in half, and the bulk-store epilogue stores
+# every tile as two 64-row halves, each into the partition holding it.
+HALF_CASES = [
+    dict(B=1, H=8, S=4608, d=128, P=8),   # the joint preset's partitions (576 rows)
+    dict(B=1, H=3, S=192, d=128, P=3),    # 64-row partitions: every tile cut
+    dict(B=2, H=4, S=640, d=64, P=2),     # 320-row partitions, d = 64, batch 2
+    dict(B=1, H=5, S=320, d=128, P=5),    # 64-row partitions, an odd tile count
+]
+
+
+@pytest.mark.parametrize("case", HALF_CASES, ids=lambda c: "B{B}H{H}S{S}d{d}P{P}".format(**c))
+def test_half_tile_bulk_stores_match_oracle_and_row_stores(case):
+    cfg = workloads.AttnConfig("halves", **case)
+    q, k, v = workloads.make_qkv(cfg, seed=9)
+    dq, dk, dv = q.cuda(), k.cuda(), v.cuda()
+    g1 = fused(dq, dk, dv, cfg.P, cfg.scale, store_kind=1)
+    assert g1.guards_intact()
+    compare(partitions_to_bhsd([p.cpu() for p in g1.parts]), orc.attention_fp64(q, k, v, cfg.scale), "half tiles")
+    g2 = fused(dq, dk, dv, cfg.P, cfg.scale, store_kind=2)
+    assert same_bytes(g1.parts, g2.parts)

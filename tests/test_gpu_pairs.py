@@ -31,6 +31,7 @@ CASES = [
     (dict(B=1, H=3, S=1000, d=128, P=3), 0),   # ragged, tiles straddling partitions
     (dict(B=2, H=3, S=640, d=128, P=1), 0),    # 3 pairs per head: the last unit half past S
     (dict(B=1, H=8, S=2304, d=128, P=8), 8),   # 4 clusters, 5 units each
+    (dict(B=1, H=8, S=4608, d=128, P=8), 0),   # 576-row partitions: tiles stored in 64-row halves
 ]
 
 

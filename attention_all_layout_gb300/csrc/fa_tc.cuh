@@ -98,10 +98,10 @@ struct Cfg {
   static constexpr int QF = 0, QE = 2, SF = 4, OF = 6, OE = 8, KVF = 10;
   static constexpr int KVE = KVF + NSTAGE;
   static constexpr int DONE = KVE + NSTAGE;
-  // bulk-store epilogue: STG = the staging buffer is free again (one phase per
-  // tile epilogue, in the order tile 0, tile 1, tile 0, ...); STGW + t = the
-  // four warps of tile t have written their rows
-  static constexpr int STG = DONE + 1, STGW = DONE + 2;
+  // store-warp epilogue: STG + t = warp 3 is done with the staging buffer
+  // after tile t's use (one phase per work item); STGW + t = the four warps of
+  // tile t have written their rows
+  static constexpr int STG = DONE + 1, STGW = DONE + 3;
   // the MMA issuer's events (see relay_role): EVA = A (the relay's arrival),
   // EVB = B_j (tile 0's 128 softmax threads + the relay), EVC = C_j and E
   // (tile 1's 128 softmax threads + the relay). Each kind's next event depends
@@ -780,13 +780,13 @@ __device__ __forceinline__ bool tile_store_target(const Params& p, const Item& w
 // ------------------------------------------------------------------ store role
 // Bulk-store modes: one thread of warp 3 issues every tile's tensor stores, so
 // that the owner warps go back to their next work as soon as they have staged
-// their rows. Epilogue uses are numbered u = 2 it + t (tile 0, then tile 1, of
-// each piece); for every use, bulk or not, it waits until the four owner warps
+// their rows. The staging buffer's uses run tile 0, then tile 1, of each
+// piece; for every use, bulk or not, it waits until the four owner warps
 // have arrived on STGW + t (after staging, or at once for a tile without bulk
 // stores or a partial piece's), issues the tile's stores and waits until they
-// have read the staging buffer, and then releases the buffer to use u + 1
-// (token STG, one phase per use). The owners of use u wait for that release of
-// use u - 1 before they arrive, so neither side gets more than one use ahead.
+// have read the staging buffer, and then releases the buffer (STG + t, one
+// phase per piece) to the next use, which waits for that release before it
+// stages (stg_free in softmax_role).
 // Before returning (also on an abort) it waits until its stores have read the
 // staging buffer: shared memory must outlive those reads, while the writes
 // themselves are complete, like any of the grid's, when the grid is.
@@ -829,7 +829,7 @@ __device__ void store_role(const Params& p, const Maps<NMAP>* maps, uint32_t stg
         bulk_commit_group();
         bulk_wait_read_all();  // the buffer may be reused once the stores have read it
       }
-      mbar_arrive(BAR(C::STG));
+      mbar_arrive(BAR(C::STG + t));
     }
   }
   bulk_wait_read_all();
@@ -957,6 +957,17 @@ __device__ void softmax_role(const Params& p, int t, uint32_t bar0, uint32_t tme
   auto BAR = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  // The staging buffer is free for this tile's use at work item `it` once
+  // warp 3 is done with the use before it, the other tile's: tile 1 waits for
+  // tile 0's release at `it`, tile 0 for tile 1's at it - 1. Each tile waits
+  // on the other tile's barrier, whose releases cannot run two phases ahead
+  // of the waiter (the other tile's next use needs this one staged first), so
+  // the parity wait is exact; one barrier for both tiles was not (a tile
+  // could wait for phase u - 1 while its own use u - 2 was still unreleased).
+  auto stg_free = [&](int item_it) -> bool {
+    if (t == 0) return item_it == 0 || mbar_wait(BAR(C::STG + 1), (item_it - 1) & 1u, w);
+    return mbar_wait(BAR(C::STG + 0), item_it & 1u, w);
+  };
   // This thread's arrival on an event of the MMA issuer (EVB, EVC, OE): a
   // pair's events are the leader's barriers, on which the other CTA arrives
   // once per warp for its 32 threads (warp-uniform call).
@@ -1087,9 +1098,8 @@ __device__ void softmax_role(const Params& p, int t, uint32_t bar0, uint32_t tme
         mbar_arrive(BAR(C::OE + t));
         if constexpr (kBulkStores<MODE>) {
           // no stores for the store role: this use only passes the staging buffer on
-          const uint32_t u = 2u * static_cast<uint32_t>(it) + static_cast<uint32_t>(t);
           if (lane == 0) {
-            if (u > 0 && !mbar_wait(BAR(C::STG), (u - 1) & 1u, w)) return;
+            if (!stg_free(it)) return;
             mbar_arrive(BAR(C::STGW + t));
           }
         }
@@ -1107,15 +1117,14 @@ __device__ void softmax_role(const Params& p, int t, uint32_t bar0, uint32_t tme
       tr_c0 = clock64();
     }
     if constexpr (kBulkStores<MODE>) {
-      // Epilogue uses are numbered u = 2 it + t; use u waits until the store
-      // role has released the staging buffer after use u - 1 (token STG, one
-      // phase per use), stages the tile when it goes out by bulk stores, and
-      // each warp arrives on STGW + t for the store role, which issues them.
-      const uint32_t u = 2u * static_cast<uint32_t>(it) + static_cast<uint32_t>(t);
+      // Each use waits until warp 3 is done with the staging buffer's
+      // previous use (stg_free), stages the tile when it goes out by bulk
+      // stores, and each warp arrives on STGW + t for the store role, which
+      // issues them.
       int map, y, z;
       const bool bulk = tile_store_target<MODE>(p, wi, t, map, y, z);
       if (bulk) {
-        if (u > 0 && !__all_sync(0xffffffffu, mbar_wait(BAR(C::STG), (u - 1) & 1u, w))) return;
+        if (!__all_sync(0xffffffffu, stg_free(it))) return;
         stage_tile<D>(stg, r, o, 1.0f / l);
         __syncwarp();
         if (lane == 0) mbar_arrive(BAR(C::STGW + t));
@@ -1124,7 +1133,7 @@ __device__ void softmax_role(const Params& p, int t, uint32_t bar0, uint32_t tme
       }
       // no bulk store for this tile: its rows go from registers below
       if (lane == 0) {
-        if (u > 0 && !mbar_wait(BAR(C::STG), (u - 1) & 1u, w)) return;
+        if (!stg_free(it)) return;
         mbar_arrive(BAR(C::STGW + t));
       }
     }
@@ -1206,7 +1215,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(BAR(C::KVE + s), 1);
     }
     mbar_init(BAR(C::DONE), 1);
-    mbar_init(BAR(C::STG), 1);
+    mbar_init(BAR(C::STG + 0), 1);
+    mbar_init(BAR(C::STG + 1), 1);
     mbar_init(BAR(C::STGW + 0), 4);  // one arrive per warp of the tile
     mbar_init(BAR(C::STGW + 1), 4);
     mbar_init(BAR(C::EVA), 1);

@@ -378,8 +378,12 @@ def main():
         pms = statistics.median(
             time_events(lambda: bd.attn_a2a_fwd(pq, pk, pv, pc.P, pc.scale, pparts, dev_status=status,
                                                 stream=stream, workspace=pws), n, 3, stream) for _ in range(3))
+        l2_note = ("back to back, no flush: q,k,v and the output (%.0f MB) fit in the 129 MB L2, so calls after "
+                   "the first find them there" % ((pc.qkv_bytes + pc.qkv_bytes / 3) / 1e6)
+                   if pc.qkv_bytes * 4 / 3 < 129e6 else
+                   "no flush: q,k,v inputs (%.2f GB) exceed the 129 MB L2" % (pc.qkv_bytes / 1e9))
         presets[name] = {"ms": pms, "tflops": pc.flops / (pms * 1e-3) / 1e12, "steps": n, "timed": when,
-                         "shape": {"B": pc.B, "H": pc.H, "S": pc.S, "d": pc.d, "P": pc.P}}
+                         "l2": l2_note, "shape": {"B": pc.B, "H": pc.H, "S": pc.S, "d": pc.d, "P": pc.P}}
         del pq, pk, pv, pparts, pws
         torch.cuda.empty_cache()
 

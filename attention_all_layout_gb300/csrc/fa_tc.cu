@@ -341,36 +341,50 @@ int launch_fa_tc(const void* q, const void* k, const void* v, const attn_a2a_sha
     p.trace = opts.trace;
     return launch_fa_tc_traced(maps, p, shp.d, mode, grid, stream);
   }
-  if (whole) return launch_fa_tc_split(maps, p, shp.d, mode, grid, stream, false);
+  // Every call's first kernel goes behind the stream's previous work with
+  // programmatic serialisation and waits for it after its set-up (kPdlWait):
+  // where that work is a kernel, its launch and set-up overlap the previous
+  // kernel's last CTAs (the next call of a short problem starts on the SMs
+  // that a call's last wave leaves idle).
+  if (whole) {
+    p.pdl = tc::kPdlWait | tc::kPdlTrigger;
+    return launch_fa_tc_split(maps, p, shp.d, mode, grid, stream, true);
+  }
   if (p.tail_first < p.total) {
     // the full waves in the plain kernel, then the tail kernel behind it
     tc::Params pm = p;
     pm.total = p.tail_first;
     pm.tail_first = pm.total;
+    pm.pdl = tc::kPdlWait;
     const int rc = launch_plain(maps, pm, shp.d, mode, grid, stream);
     if (rc != ATTN_A2A_OK) return rc;
+    p.pdl = tc::kPdlWaitEnd;
     return launch_fa_tc_split(maps, p, shp.d, mode, grid, stream, true);
   }
+  p.pdl = tc::kPdlWait;
   return launch_plain(maps, p, shp.d, mode, grid, stream);
 }
 
+// The plain kernel, launched with programmatic serialisation when p.pdl asks
+// its CTAs to wait for the stream's previous kernel.
 int launch_plain(const tc::Maps<1>& maps, const tc::Params& p, int d, int mode, int grid, cudaStream_t stream) {
+  const bool pdl = (p.pdl & tc::kPdlWait) != 0;
   switch (mode) {
     case tc::kModeA2AT:
-      return d == 128 ? launch_t<128, tc::kModeA2AT, 1>(maps, p, grid, stream)
-                      : launch_t<64, tc::kModeA2AT, 1>(maps, p, grid, stream);
+      return d == 128 ? launch_t<128, tc::kModeA2AT, 1>(maps, p, grid, stream, pdl)
+                      : launch_t<64, tc::kModeA2AT, 1>(maps, p, grid, stream, pdl);
     case tc::kModeContigT:
-      return d == 128 ? launch_t<128, tc::kModeContigT, 1>(maps, p, grid, stream)
-                      : launch_t<64, tc::kModeContigT, 1>(maps, p, grid, stream);
+      return d == 128 ? launch_t<128, tc::kModeContigT, 1>(maps, p, grid, stream, pdl)
+                      : launch_t<64, tc::kModeContigT, 1>(maps, p, grid, stream, pdl);
     case tc::kModeA2A:
-      return d == 128 ? launch_t<128, tc::kModeA2A, 1>(maps, p, grid, stream)
-                      : launch_t<64, tc::kModeA2A, 1>(maps, p, grid, stream);
+      return d == 128 ? launch_t<128, tc::kModeA2A, 1>(maps, p, grid, stream, pdl)
+                      : launch_t<64, tc::kModeA2A, 1>(maps, p, grid, stream, pdl);
     case tc::kModeA2AC:
-      return d == 128 ? launch_t<128, tc::kModeA2AC, 1>(maps, p, grid, stream)
-                      : launch_t<64, tc::kModeA2AC, 1>(maps, p, grid, stream);
+      return d == 128 ? launch_t<128, tc::kModeA2AC, 1>(maps, p, grid, stream, pdl)
+                      : launch_t<64, tc::kModeA2AC, 1>(maps, p, grid, stream, pdl);
     default:
-      return d == 128 ? launch_t<128, tc::kModeContig, 1>(maps, p, grid, stream)
-                      : launch_t<64, tc::kModeContig, 1>(maps, p, grid, stream);
+      return d == 128 ? launch_t<128, tc::kModeContig, 1>(maps, p, grid, stream, pdl)
+                      : launch_t<64, tc::kModeContig, 1>(maps, p, grid, stream, pdl);
   }
 }
 
@@ -446,22 +460,29 @@ int launch_fa_tc_s2s(const void* const* qp, const void* const* kp, const void* c
           return ATTN_A2A_ECUDA;
     }
     const int mode = kind == 1 ? tc::kModeS2SGT : tc::kModeS2SG;
+    // programmatic serialisation behind the stream's previous kernel, as in launch_fa_tc
     auto plain = [&](const tc::Params& pp) -> int {
       if (kind == 1)
-        return shp.d == 128 ? launch_t<128, tc::kModeS2SGT, tc::kMaxS2SRanks>(maps, pp, grid, stream)
-                            : launch_t<64, tc::kModeS2SGT, tc::kMaxS2SRanks>(maps, pp, grid, stream);
-      return shp.d == 128 ? launch_t<128, tc::kModeS2SG, tc::kMaxS2SRanks>(maps, pp, grid, stream)
-                          : launch_t<64, tc::kModeS2SG, tc::kMaxS2SRanks>(maps, pp, grid, stream);
+        return shp.d == 128 ? launch_t<128, tc::kModeS2SGT, tc::kMaxS2SRanks>(maps, pp, grid, stream, true)
+                            : launch_t<64, tc::kModeS2SGT, tc::kMaxS2SRanks>(maps, pp, grid, stream, true);
+      return shp.d == 128 ? launch_t<128, tc::kModeS2SG, tc::kMaxS2SRanks>(maps, pp, grid, stream, true)
+                          : launch_t<64, tc::kModeS2SG, tc::kMaxS2SRanks>(maps, pp, grid, stream, true);
     };
-    if (whole) return launch_fa_tc_split_s2s(maps, p, shp.d, mode, grid, stream, false);
+    if (whole) {
+      p.pdl = tc::kPdlWait | tc::kPdlTrigger;
+      return launch_fa_tc_split_s2s(maps, p, shp.d, mode, grid, stream, true);
+    }
     if (p.tail_first < p.total) {
       tc::Params pm = p;
       pm.total = p.tail_first;
       pm.tail_first = pm.total;
+      pm.pdl = tc::kPdlWait;
       const int rc = plain(pm);
       if (rc != ATTN_A2A_OK) return rc;
+      p.pdl = tc::kPdlWaitEnd;
       return launch_fa_tc_split_s2s(maps, p, shp.d, mode, grid, stream, true);
     }
+    p.pdl = tc::kPdlWait;
     return plain(p);
   }
   p.nb_big = (epi.cbase + 1 + tc::kBM - 1) / tc::kBM;
@@ -471,10 +492,11 @@ int launch_fa_tc_s2s(const void* const* qp, const void* const* kp, const void* c
   p.total = shp.B * shp.H * p.npair;
   p.epi = epi;
   p.tail_first = p.total;  // no split schedule with per-partition tiles
+  p.pdl = tc::kPdlWait;
   const int grid = grid_for(p, opts);
   if (grid <= 0) return ATTN_A2A_ECUDA;
-  if (shp.d == 128) return launch_t<128, tc::kModeS2S, tc::kMaxS2SRanks>(maps, p, grid, stream);
-  return launch_t<64, tc::kModeS2S, tc::kMaxS2SRanks>(maps, p, grid, stream);
+  if (shp.d == 128) return launch_t<128, tc::kModeS2S, tc::kMaxS2SRanks>(maps, p, grid, stream, true);
+  return launch_t<64, tc::kModeS2S, tc::kMaxS2SRanks>(maps, p, grid, stream, true);
 }
 
 }  // namespace attn_a2a

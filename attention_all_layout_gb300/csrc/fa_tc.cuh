@@ -179,6 +179,19 @@ struct Maps {
   CUtensorMap o[kMaxStoreMaps];  // output partitions, bulk-store epilogue only
 };
 
+// Params::pdl (programmatic dependent launch). kPdlWait: the kernel was
+// launched with programmatic stream serialisation behind whatever ran before
+// it on the stream, and every thread waits for that grid's completion
+// (griddepcontrol.wait) after the set-up and before its first access to
+// global memory. kPdlTrigger: a split kernel lets the next kernel of the
+// stream launch once all its CTAs have started
+// (griddepcontrol.launch_dependents); the plain kernel always does.
+// kPdlWaitEnd: the tail kernel, which runs beside the plain kernel ahead of
+// it without waiting for it, waits for it before exiting, so that the tail
+// kernel's completion - all that a kernel queued behind it with programmatic
+// serialisation waits for - covers the plain kernel's stores too.
+constexpr int kPdlWait = 1, kPdlTrigger = 2, kPdlWaitEnd = 4;
+
 struct Params {
   int B, H, S;
   int nblk;   // query tiles per head = key blocks per head (ceil(S/128), or the per-partition count)
@@ -195,6 +208,7 @@ struct Params {
   int half_stores;       // kModeA2AT, kModeS2SGT: every tile stored as two 64-row halves, each into the partition
                          // holding it (equal partitions of an odd multiple of 64 rows; 64-row output boxes)
   long long* trace;      // traced instantiations only: kTraceRecord int64 per (item, tile, warp)
+  int pdl;               // kPdlWait | kPdlTrigger: programmatic dependent launch (see the kernel's set-up)
   // Split schedule (see tail_piece): the key blocks of items [tail_first,
   // total) are divided over the CTAs, tail_len blocks per CTA; tail_first =
   // total when nothing is split. Partial results go through the caller's
@@ -1253,9 +1267,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   if constexpr (PAIR) cluster_sync();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // a tail kernel queued behind this one may launch now: it takes each SM
-  // as this kernel's CTA there exits (no effect without one)
-  if constexpr (!SPLIT) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // A kernel queued behind this one with programmatic serialisation may
+  // launch now (no effect without one): a tail kernel takes each SM as this
+  // kernel's CTA there exits; the next call's first kernel runs its set-up
+  // there and waits. A dependent grid launches only once every CTA of this
+  // one has started, so its waiting CTAs never keep one of this grid's off
+  // an SM (a split kernel's ranges must all be resident at once).
+  if (!SPLIT || (p.pdl & kPdlTrigger)) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // Launched behind the previous kernel of the stream: the set-up above
+  // overlapped its last CTAs; nothing global is touched before it has
+  // completed and its memory operations are visible.
+  if (p.pdl & kPdlWait) asm volatile("griddepcontrol.wait;" ::: "memory");
   const WaitCtl w{abort_flag, p.dev_status, p.timeout_ns};
 
   if (warp < 4) {
@@ -1275,6 +1297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
     softmax_role<D, MODE, NMAP, TRACE, SPLIT, PAIR>(p, (warp - 4) / 4, bar0, tmem, &maps, sbase + C::STG_OFF, w);
   }
+  if (p.pdl & kPdlWaitEnd) asm volatile("griddepcontrol.wait;" ::: "memory");
   tc_fence_before();
   __syncthreads();
   // a pair: the leader's MMAs read the other CTA's shared memory and TMEM,

@@ -56,8 +56,9 @@ int launch_t(const tc::Maps<NMAP>& maps, const tc::Params& p, int grid, cudaStre
     return ATTN_A2A_OK;
   }
   if (pdl) {
-    // the tail kernel, queued behind the plain one: launched with programmatic
-    // stream serialisation, so its CTAs start as the plain kernel's CTAs exit
+    // launched with programmatic stream serialisation: the tail kernel's CTAs
+    // start as the plain kernel's CTAs exit; a call's first kernel (p.pdl has
+    // kPdlWait) runs its set-up as the previous kernel's CTAs exit and waits
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(tc::kThreads);
@@ -84,9 +85,10 @@ int launch_fa_tc_traced(const tc::Maps<1>& maps, const tc::Params& p, int d, int
                         cudaStream_t stream);
 
 // The split instantiation (pieces of items tail_first .. total - 1, workspace
-// in p) of the same four modes: with pdl, the tail kernel launched behind the
-// plain kernel that runs items 0 .. tail_first - 1; without, the whole
-// schedule on its own.
+// in p) of the same four modes: the tail kernel behind the plain kernel that
+// runs items 0 .. tail_first - 1, or the whole schedule on its own; with
+// pdl, launched with programmatic stream serialisation (p.pdl says what the
+// kernel waits for).
 int launch_fa_tc_split(const tc::Maps<1>& maps, const tc::Params& p, int d, int mode, int grid,
                        cudaStream_t stream, bool pdl);
 

@@ -35,7 +35,15 @@
  *     events of attn_a2a_fwd_host), plus the fixed __device__ array of
  *     xstage_probe_run_noalloc.
  *   - Streams: `stream` is a cudaStream_t passed as void* (NULL = the legacy
- *     default stream). Work is asynchronous on that stream.
+ *     default stream). Work is asynchronous on that stream and ordered with
+ *     it as any kernel is. The attention calls launch their first kernel with
+ *     programmatic stream serialisation: where the stream's previous work is
+ *     a kernel that allows it (CUDA's programmatic dependent launch), their
+ *     CTAs may start on SMs that kernel has left and run their set-up, but
+ *     they wait for that kernel's completion before they read or write any
+ *     buffer. A kernel the caller queues behind a call with programmatic
+ *     serialisation waits, as usual, for the call's last kernel, whose
+ *     completion covers all of the call's stores.
  *   - Errors: argument errors are detected on the host and returned
  *     synchronously before anything is launched (ATTN_A2A_EINVAL /
  *     ATTN_A2A_EUNSUPPORTED). A launch failure returns ATTN_A2A_ECUDA.

@@ -12,7 +12,9 @@ up. Both outputs must be byte-identical to the same two calls each followed
 by a device synchronisation - for the plain kernel alone (a partial last wave,
 so that most CTAs exit early and the next call's CTAs start beside the last
 ones), the plain kernel with the tail kernel behind it, and the
-whole-schedule split, with both store kinds.
+whole-schedule split, with both store kinds; the same for the fused call
+behind attention alone, and for two whole-layer calls (sequence-sharded in
+and out), the second reading the first one's output partitions.
 """
 import pytest
 import torch
@@ -83,3 +85,40 @@ def test_fused_call_behind_attention_alone():
     torch.cuda.synchronize()
     for a, b in zip(parts, ref):
         assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+@pytest.mark.parametrize("split", [bd.SPLIT_NONE, bd.SPLIT_ALL])
+def test_layer_call_reads_the_previous_layer_calls_output(split):
+    """The whole layer (sequence-sharded q, k, v in and out): a second call whose q
+    partitions are the first call's output partitions, queued right behind it."""
+    cfg = workloads.AttnConfig("chain", B=B, H=H, S=S, d=D, P=4)
+    q, k, v = (t.cuda() for t in workloads.make_qkv(cfg, seed=13))
+    qp, kp, vp = (bd.alloc_partitions(B, S, H, D, cfg.P) for _ in range(3))
+    for src, dst in ((q, qp), (k, kp), (v, vp)):
+        bd.attn_a2a_permute(src, cfg.P, dst)
+    ws = bd.alloc_workspace(D, GRID)
+    torch.cuda.synchronize()
+
+    def layer(qparts, out):
+        bd.attn_a2a_fwd_s2s(qparts, kp, vp, cfg.P, cfg.scale, out, grid=GRID, workspace=ws, split=split)
+
+    def nan_parts():
+        parts = bd.alloc_partitions(B, S, H, D, cfg.P)
+        for p in parts:
+            p.fill_(float("nan"))
+        return parts
+
+    ref1, ref2 = nan_parts(), nan_parts()
+    layer(qp, ref1)
+    torch.cuda.synchronize()
+    layer(ref1, ref2)
+    torch.cuda.synchronize()
+    assert not any(bool(torch.isnan(p).any()) for p in ref1 + ref2)
+    for _ in range(3):
+        o1, o2 = nan_parts(), nan_parts()
+        torch.cuda.synchronize()
+        layer(qp, o1)
+        layer(o1, o2)
+        torch.cuda.synchronize()
+        for a, b in zip(o1 + o2, ref1 + ref2):
+            assert torch.equal(a.view(torch.int16), b.view(torch.int16))
